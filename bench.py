@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the fused ZeRO shard step on one GB300 (or N replicas).
+
+One step = one fused zero_step over all virtual ranks of the BERT-base-sized
+flat group: reduce-scatter of 8 bf16 gradient replicas, AdamW on the fp32
+master/m/v shards, bf16 cast and all-gather into the flat parameter buffer.
+
+Prints one JSON line (rank 0).  `value` is whole-job params/s with inputs
+resident in HBM; `e2e` is the same metric through the public API with the
+gradients copied from pinned host memory and the updated parameters copied
+back every step; `roofline` relates the kernel's algorithmic bytes to the
+measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle on a bounded
+sample.  `--impl reference` times the oracle alone (the reference arm).
+
+Multi-GPU (`torchrun --nproc-per-node N bench.py --gpus N`): every rank runs
+its own full replica of the workload (the virtual ranks live inside one GPU;
+there is no data-path collective), timing is max-over-ranks, value sums the
+work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "bert_base"
+METRIC = "fused ZeRO shard step: params/s and HBM GB/s (fraction of GB300 peak)"
+UNIT = "params/s"
+KERNEL_PREFIX = "k_step"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (host side; no data-path collective)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is None:
+        return
+    if device is not None:
+        dist.barrier(device_ids=[device])
+    else:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest `value` over all ranks (timing only)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=f"cuda:{device}" if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []  # (host time, fields)
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError) as e:
+            self.error = f"nvidia-smi unavailable: {e}"
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.error}
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if not win:
+            win = [p for (_, p) in self.samples]
+            note = "no sample fell inside the timed region; all samples of the run"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        reasons = sorted({name for p in win for name, val in zip(self.REASONS, p[5:9])
+                          if val.lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(win)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ----------------------------------------------------------------------------
+# helpers
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "zero_sharded_optimizer_flatten_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def step_bytes(phi_padded: int, n_ranks: int, zero3: bool = False) -> int:
+    """Algorithmic HBM bytes of one fused step: per element N 16-bit gradient
+    reads, master/m/v read + write (24 B), one 16-bit parameter write."""
+    per = 2 * n_ranks + 24 + 2 + (2 if zero3 else 0)
+    return per * phi_padded
+
+
+# ----------------------------------------------------------------------------
+# the oracle as a CPU baseline
+
+
+class OracleSample:
+    """The CPU oracle's element step on the first n elements of the workload
+    (all gradient replicas), inputs drawn once on the CPU; step(t) times one
+    oracle call, nothing else."""
+
+    def __init__(self, w, n_elems: int):
+        import numpy as np
+        import torch
+
+        import oracle
+        from zero_sharded_optimizer_flatten_gb300 import workloads as W
+        torch.set_num_threads(1)
+        self.oracle, self.w, self.n = oracle, w, n_elems
+        self.dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
+        self.op = oracle.AVG if w.op == "avg" else oracle.SUM
+        p16 = W.fill(w, "param", 0, 0, 0, n_elems, torch.empty(n_elems, dtype=w.torch_dtype))
+        self.grads = np.stack([W.grads16(w, 1, q, "cpu", 0, n_elems).view(torch.int16).numpy()
+                               .view(np.uint16) for q in range(w.n_ranks)])
+        self.master = oracle.to_f32(p16.view(torch.int16).numpy().view(np.uint16), self.dt)
+        self.m = np.zeros_like(self.master)
+        self.v = np.zeros_like(self.master)
+        self.out = np.zeros(n_elems, np.uint16)
+        self.hp = oracle.hparams()
+
+    def step(self, t: int) -> float:
+        t0 = time.perf_counter()
+        self.oracle.update_elements(self.grads, self.master, self.m, self.v, self.dt, self.op,
+                                    self.hp, t, out16=self.out)
+        return time.perf_counter() - t0
+
+
+def oracle_rate(w, n_elems: int):
+    el = OracleSample(w, n_elems).step(1)
+    return n_elems / el, el
+
+
+def cpu_baseline(w, budget_s: float = 10.0):
+    rate, _ = oracle_rate(w, 1 << 16)
+    n = int(min(w.phi, max(1 << 16, rate * budget_s)))
+    n -= n % 8
+    rate, el = oracle_rate(w, n)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} elements of the {w.key} group (all {w.n_ranks} gradient replicas), "
+                      f"one step of the single-threaded C oracle, {el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------
+# arms
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    if rank != 0:
+        return 0
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD]
+    rate, _ = oracle_rate(w, 1 << 16)
+    total_budget = 60.0
+    n = int(rate * total_budget / max(1, args.steps + args.warmup))
+    n = max(4096, min(n, w.phi))
+    n -= n % 8
+    sample = OracleSample(w, n)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        sample.step(t)
+    els = []
+    for _ in range(args.steps):
+        t += 1
+        els.append(sample.step(t))
+    tot = sum(els)
+    value = n * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": W.WORKLOADS[WORKLOAD].title, "phi": w.phi,
+                   "virtual_ranks": w.n_ranks, "sample_elements_per_step": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} of {w.phi} elements per step, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import zero_sharded_optimizer_flatten_gb300 as Z
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    w = W.WORKLOADS[WORKLOAD]
+    dev = torch.device("cuda", local)
+    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+    P = plan.padded
+    hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+    p16 = W.params16(w, dev)
+    full16 = torch.zeros_like(p16)
+    S = [plan.shard_len(r) for r in range(w.n_ranks)]
+    master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+    m = [torch.empty_like(x) for x in master]
+    v = [torch.empty_like(x) for x in master]
+    Z.zero_init_shards(plan, p16, master, m, v)
+    n_sets = 2  # distinct gradient sets, alternated step to step
+    grads = [[W.grads16(w, s + 1, q, dev) for q in range(w.n_ranks)] for s in range(n_sets)]
+    steps = [Z.ZeroStep(plan, g, w.op, master, m, v, full16, None, hp) for g in grads]
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        steps[t % n_sets](t)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(dist, local)
+    torch.cuda.synchronize(dev)
+    launches0 = Z.zero_launch_count()
+    wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        t += 1
+        ev[k][0].record(stream)
+        steps[t % n_sets](t)
+        ev[k][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    launches = Z.zero_launch_count() - launches0
+    barrier(dist, local)
+    clocks.stop()
+    elapsed = start.elapsed_time(stop) / 1e3
+    elapsed = max_over_ranks(dist, elapsed, local)
+    kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
+
+    # end to end through the public API: pinned host gradients in, updated
+    # parameters out, every step
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    host_g = [torch.empty(P, dtype=w.torch_dtype, pin_memory=True) for _ in range(w.n_ranks)]
+    for q in range(w.n_ranks):
+        host_g[q].copy_(grads[0][q])
+    host_out = torch.empty(P, dtype=w.torch_dtype, pin_memory=True)
+    dev_g = grads[0]
+    for _ in range(2):
+        t += 1
+        for q in range(w.n_ranks):
+            dev_g[q].copy_(host_g[q], non_blocking=True)
+        Z.zero_step(plan, dev_g, w.op, master, m, v, full16, None, hp, t)
+        host_out.copy_(full16, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(dist, local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        t += 1
+        for q in range(w.n_ranks):
+            dev_g[q].copy_(host_g[q], non_blocking=True)
+        Z.zero_step(plan, dev_g, w.op, master, m, v, full16, None, hp, t)
+        host_out.copy_(full16, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(dist, e0.elapsed_time(e1) / 1e3, local)
+
+    bytes_per_launch = step_bytes(P, w.n_ranks)
+    peak, peak_src = measured_peaks()
+    achieved = bytes_per_launch / kernel_s / 1e9
+    line = {
+        "impl": "gb300",
+        "metric": METRIC,
+        "value": w.phi * args.steps * world / elapsed,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.title,
+            "phi": w.phi,
+            "padded": P,
+            "virtual_ranks": w.n_ranks,
+            "storage": "bf16 params and gradients, fp32 master/m/v",
+            "parallelism": f"{world} independent replica(s); {w.n_ranks} virtual ranks each",
+            "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB touched per step",
+            "hbm_gbs_per_step": bytes_per_launch / (elapsed / args.steps) / 1e9,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": recorded_traffic(WORKLOAD),
+            "kernel": KERNEL_PREFIX,
+            "bytes_per_launch": bytes_per_launch,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                           else "fallback 6.8 TB/s",
+        },
+        "e2e": {
+            "value": w.phi * e2e_steps * world / e2e_s,
+            "unit": UNIT,
+            "h2d_bytes_per_step": w.n_ranks * P * 2,
+            "d2h_bytes_per_step": P * 2,
+            "steps": e2e_steps,
+        },
+        "gpu_launches": launches,
+        "clocks": clocks.summary(wall0, wall1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

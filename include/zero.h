@@ -1,0 +1,239 @@
+/*
+ * zero.h -- C ABI of the GB300 ZeRO sharded mixed-precision optimizer step.
+ *
+ * One process, one GPU, N *virtual* data-parallel ranks: rank q's gradient
+ * replica and rank r's optimizer shard are separate caller-owned buffers in
+ * the same HBM.  The library owns only the partition plan (host memory).
+ * Every tensor argument is caller-owned device memory (for example a torch
+ * tensor's data_ptr()); every stream argument is a cudaStream_t passed as
+ * void* (NULL = the legacy default stream).  Compute calls are asynchronous
+ * on that stream.
+ *
+ * Sources (page title, section) for what each call computes:
+ *  [ZeRO-2 blog]   "DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com):
+ *                  §2.1 and §4.1 flatten + near-equal partition + fp32 master
+ *                  cloned from the 16-bit partition; §2.2 and §4.2 bucketed
+ *                  reduce-scatter leaving each rank the averaged gradient of
+ *                  its partition; §4.3 local update of the rank's partition;
+ *                  §4.4 all-gather of the updated partitions.
+ *  [cookllm ZeRO]  "ZeRO 优化器" (cookllm.com): 参数分配策略 (tensor i owned
+ *                  by rank i % world_size), 梯度同步 (reduce = sum to the
+ *                  owner), the per-stage memory tables.
+ *  [ZeRO report]   "ZeRO / DeepSpeed 深度解读报告" (zako-mio.github.io) §3.3:
+ *                  per-device memory 16P, 4P+12P/N, 2P+14P/N, 16P/N.
+ *  [wmrh tutorial] "ZeRO ... 实操" (wmrh.cn) §3.1: AdamW hyper-parameters.
+ *
+ * Conventions common to every call:
+ *  - Every call returns a zero_status and never throws or aborts.  On
+ *    failure, zero_last_error() returns a message (thread-local storage,
+ *    valid until the next call on the same thread).
+ *  - All arguments are validated before anything is launched; a call that
+ *    fails validation launches nothing and leaves every output untouched.
+ *  - Device pointers must be 16-byte aligned (ZERO_ERR_ALIGN otherwise);
+ *    torch allocations are 256-byte aligned.
+ *  - Asynchronous device errors surface as ZERO_ERR_CUDA from the next call
+ *    or from zero_sync().
+ *  - At most 64 virtual ranks; rank_mask bit r selects rank r.  Pointer
+ *    arrays are indexed by rank and have n_ranks entries; entries of ranks
+ *    outside rank_mask, or whose shard is empty, are not read and may be
+ *    NULL.
+ *  - Flat indices f run over the gathered flat buffer (length `padded` from
+ *    zero_plan_total); shard indices i run over rank r's shard buffers
+ *    (length from zero_plan_shard).
+ */
+#ifndef ZERO_GB300_H_
+#define ZERO_GB300_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZERO_OK = 0,
+  ZERO_ERR_INVALID = 1,     /* bad argument: null, out of range, size mismatch   */
+  ZERO_ERR_ALIGN = 2,       /* a device pointer is not 16-byte aligned           */
+  ZERO_ERR_CUDA = 3,        /* CUDA runtime error (launch or asynchronous)       */
+  ZERO_ERR_OOM = 4,         /* host allocation failed                            */
+  ZERO_ERR_TIMEOUT = 5,     /* reserved: no call waits on the device             */
+  ZERO_ERR_UNSUPPORTED = 6  /* valid request this build does not implement       */
+} zero_status;
+
+typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype;
+typedef enum { ZERO_PART_FLAT = 0, ZERO_PART_ROUND_ROBIN = 1 } zero_part_mode;
+typedef enum { ZERO_REDUCE_SUM = 0, ZERO_REDUCE_AVG = 1 } zero_reduce_op;
+
+/*
+ * AdamW hyper-parameters as the caller holds them (binary64).  The library
+ * forms the step's binary32 constants in binary64 and rounds each once:
+ *   d = 1 - lr*weight_decay, c1 = 1 - beta1, c2 = 1 - beta2,
+ *   ss = lr / (1 - beta1^t), sb = sqrt(1 - beta2^t).
+ * Requirements: all finite, lr >= 0, weight_decay >= 0, eps > 0,
+ * 0 <= beta1 < 1, 0 <= beta2 < 1.
+ */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+} zero_adamw_hparams;
+
+typedef struct zero_plan zero_plan; /* opaque, host memory, owned by the library */
+
+/* ------------------------------------------------------------------------ */
+/* Partition plan (host only; no GPU needed)                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Build the partition plan of one parameter group.
+ *  numel[k], k < n_tensors: element counts of the group's tensors in
+ *    named_parameters() order (>= 0; n_tensors >= 1).
+ *  ZERO_PART_FLAT ([ZeRO-2 blog] §2.1, §4.1): the tensors are concatenated
+ *    with no gap into one flat buffer of phi = sum(numel) elements, padded at
+ *    the tail with zeros to P = ceil(phi / (n_ranks*align_elems)) *
+ *    n_ranks*align_elems; rank r owns flat range [r*S, (r+1)*S), S = P/n_ranks.
+ *    align_elems must be a power of two in [1, 4096].
+ *  ZERO_PART_ROUND_ROBIN ([cookllm ZeRO] 参数分配策略): tensor k is owned
+ *    whole by rank k % n_ranks; the flat buffer is the unpadded concatenation
+ *    (P = phi) and rank r's shard packs its tensors in increasing k.
+ *    align_elems is ignored.
+ *  n_ranks in [1, 64].  On success *out receives a plan that the caller
+ *  releases with zero_plan_destroy.
+ */
+zero_status zero_plan_partitions(const int64_t* numel, int32_t n_tensors, int32_t n_ranks,
+                                 zero_part_mode mode, int32_t align_elems, zero_plan** out);
+
+/* Release a plan (NULL is allowed). */
+void zero_plan_destroy(zero_plan* plan);
+
+/* phi = real element count, padded = length of the gathered flat buffer. */
+zero_status zero_plan_total(const zero_plan* plan, int64_t* phi, int64_t* padded);
+
+/* Number of virtual ranks and the partition mode of a plan. */
+zero_status zero_plan_info(const zero_plan* plan, int32_t* n_ranks, int32_t* mode,
+                           int32_t* align_elems, int32_t* n_tensors);
+
+/*
+ * Rank r's shard: *len = its element count; *flat_off = the flat index of its
+ * first element in flat mode, or -1 in round-robin mode (shards are not
+ * contiguous in the flat buffer there).
+ */
+zero_status zero_plan_shard(const zero_plan* plan, int32_t rank, int64_t* flat_off,
+                            int64_t* len);
+
+/*
+ * Ownership map of rank r: the segments (tensor_idx, tensor_off, flat_off,
+ * shard_off, len) in increasing flat order.  A segment is a maximal run of
+ * elements that lies in one tensor and in rank r's shard; flat-mode tail
+ * padding is reported with tensor_idx = -1.  Each output array holds `cap`
+ * entries; *n_out receives the number of segments (which may exceed cap: call
+ * once with cap = 0 to size the arrays).  Output arrays may be NULL when
+ * cap == 0.
+ */
+zero_status zero_plan_segments(const zero_plan* plan, int32_t rank, int64_t* tensor_idx,
+                               int64_t* tensor_off, int64_t* flat_off, int64_t* shard_off,
+                               int64_t* len, int64_t cap, int64_t* n_out);
+
+/* Human-readable dump of the plan into buf (NUL-terminated, truncated to cap). */
+zero_status zero_plan_describe(const zero_plan* plan, char* buf, int64_t cap);
+
+/*
+ * Per-rank model-state bytes of mixed-precision Adam training ([ZeRO report]
+ * §3.3; [cookllm ZeRO] stage tables): 2 B/param 16-bit params, 2 B/param
+ * 16-bit grads, 12 B/param fp32 master + m + v.  stage 0 (DDP) 16 phi;
+ * 1: 4 phi + 12 phi/N; 2: 2 phi + 14 phi/N; 3: 16 phi/N.  Returned as the
+ * exact reduced fraction *num / *den.  ZERO_ERR_INVALID if the numerator
+ * would overflow int64.
+ */
+zero_status zero_memory_bytes(int32_t stage, int64_t phi, int32_t n_ranks, int64_t* num,
+                              int64_t* den);
+
+/* ------------------------------------------------------------------------ */
+/* Device calls                                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Optimizer-state initialisation ([ZeRO-2 blog] §4.1: each rank clones its
+ * fp32 master from its own 16-bit partition):
+ *   master[r][i] = float(full_flat16[f]), m[r][i] = v[r][i] = +0
+ * for every (f, i) owned by a rank in rank_mask.  The widening is exact.
+ *  full_flat16: device, `padded` 16-bit elements of `dtype` (read).
+ *  master/m/v:  n_ranks device pointers, each to that rank's shard length of
+ *               float (written).
+ */
+zero_status zero_init_shards(const zero_plan* plan, const void* full_flat16, zero_dtype dtype,
+                             float* const* master, float* const* m, float* const* v,
+                             uint64_t rank_mask, void* stream);
+
+/*
+ * Reduce-scatter ([ZeRO-2 blog] §2.2, §4.2; [cookllm ZeRO] 梯度同步):
+ *   grad_shards[r][i] = G_0[f] + G_1[f] + ... + G_{N-1}[f]
+ * accumulated in binary32 in rank order, then divided by N for
+ * ZERO_REDUCE_AVG.  grads[q] (n_ranks entries, all required) points to rank
+ * q's flat gradient replica of `dtype`; it is read only at the flat indices
+ * owned by ranks in rank_mask (so a caller holding only those ranges may pass
+ * correspondingly offset pointers).  grad_shards[r]: device float[shard len].
+ *  bucket_elems > 0 splits the work into buckets of that many flat indices,
+ *  one launch each (like the reduce_bucket_size of the pages); <= 0 means one
+ *  bucket.  Results do not depend on the bucketing.
+ */
+zero_status zero_reduce_scatter(const zero_plan* plan, const void* const* grads,
+                                zero_dtype dtype, zero_reduce_op op, float* const* grad_shards,
+                                uint64_t rank_mask, int64_t bucket_elems, void* stream);
+
+/*
+ * Local AdamW step on each masked rank's shard ([ZeRO-2 blog] §4.3), one
+ * binary32 rounding per operation, in this order (t = step >= 1):
+ *   p = p*d;  m = b1*m + c1*g;  v = b2*v + c2*(g*g);
+ *   den = sqrt(v)/sb + eps;  p = p - ss*(m/den)
+ * and, when out16_shard is non-NULL, out16_shard[r][i] = p rounded to
+ * nearest even in `dtype` (entries may be NULL to skip a rank).
+ *  master/m/v: device float[shard len] (read-modify-write).
+ *  grad_shards: device float[shard len] (read).
+ */
+zero_status zero_adamw_shard_step(const zero_plan* plan, float* const* master, float* const* m,
+                                  float* const* v, const float* const* grad_shards,
+                                  void* const* out16_shard, zero_dtype dtype,
+                                  const zero_adamw_hparams* hp, int64_t step,
+                                  uint64_t rank_mask, void* stream);
+
+/*
+ * All-gather ([ZeRO-2 blog] §4.4): full_flat16[f] = shards16[r][i] for every
+ * (f, i) owned by a rank in rank_mask.  Flat-mode tail padding belongs to
+ * the last rank's shard and is copied like any other element.
+ */
+zero_status zero_allgather(const zero_plan* plan, const void* const* shards16,
+                           zero_dtype dtype, void* full_flat16, uint64_t rank_mask,
+                           void* stream);
+
+/*
+ * The fused step: reduce-scatter, AdamW, cast and all-gather in one pass
+ * over HBM (one read of the N gradient replicas and of master/m/v, one write
+ * of master/m/v and of the 16-bit parameters).  The results are bit-identical
+ * to zero_reduce_scatter -> zero_adamw_shard_step -> zero_allgather.
+ *  full_flat16 (nullable): gathered flat 16-bit buffer, written at the flat
+ *    indices of masked ranks.
+ *  out16_shard (nullable, entries nullable): each rank's 16-bit shard (the
+ *    ZeRO-3 layout, where the shard is the next all-gather's source).
+ *  bucket_elems: as for zero_reduce_scatter.
+ */
+zero_status zero_step(const zero_plan* plan, const void* const* grads, zero_dtype dtype,
+                      zero_reduce_op op, float* const* master, float* const* m, float* const* v,
+                      void* full_flat16, void* const* out16_shard, const zero_adamw_hparams* hp,
+                      int64_t step, uint64_t rank_mask, int64_t bucket_elems, void* stream);
+
+/* Synchronize `stream` and report any asynchronous device error. */
+zero_status zero_sync(void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* zero_last_error(void);
+
+/* Number of kernel launches the library issued since load (all threads). */
+int64_t zero_launch_count(void);
+
+/* Library version string. */
+const char* zero_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H_ */

@@ -1,0 +1,310 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small groups are compared element by element over whole buffers; the five
+named parameter groups at full size are compared on sampled elements (seeded
+random indices plus every shard, tensor, tile and bucket edge), which the
+oracle recomputes one by one from the same inputs.  The launch configuration
+is the one the benchmark uses (the library picks it; nothing here changes it).
+
+Pass criteria: partition layout and gathered buffers bit-exact; fp32
+master/m/v within 1e-6 relative error; 16-bit parameters within 1 ulp.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._harness import (Case, assert_16_close, assert_fp32_close, dt_code, f32,
+                            hp_oracle, op_code, owner_of, sample_indices, u16)
+from zero_sharded_optimizer_flatten_gb300 import workloads as W
+from zero_sharded_optimizer_flatten_gb300 import zero as Z
+
+pytestmark = pytest.mark.gpu
+
+HP = Z.AdamW(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+@pytest.fixture(autouse=True)
+def _cuda_cleanup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _run_full(w: W.Workload, steps: int, hp=HP, bucket=0, stream=None):
+    c = Case(w)
+    for t in range(1, steps + 1):
+        g = c.grads(t)
+        Z.zero_step(c.plan, g, w.op, c.master, c.m, c.v, c.full16, None, hp, t,
+                    rank_mask=w.mask, bucket_elems=bucket, stream=stream)
+        c.oracle_step(g, t, hp_oracle(hp))
+    torch.cuda.synchronize()
+    c.compare(f"{w.key} step {steps}")
+    return c
+
+
+# ----------------------------------------------------------------------------
+# whole-buffer parity
+
+
+def test_tiny_mlp_group_full():
+    """The tiny-MLP group (1,053,706 params, fp16, N=4, A=16), 3 steps."""
+    _run_full(W.WORKLOADS["tiny_mlp"], 3)
+
+
+SMALL = [
+    # numel, N, mode, A, dtype, op
+    ((1000, 37, 4096, 3, 129, 0, 8191), 4, "flat", 16, "fp16", "avg"),
+    ((1000, 37, 4096, 3, 129, 0, 8191), 4, "flat", 16, "bf16", "sum"),
+    ((1000, 37, 4096, 3, 129, 0, 8191), 3, "flat", 2, "bf16", "avg"),   # unaligned shards
+    ((1000, 37, 4096, 3, 129, 0, 8191), 5, "flat", 1, "fp16", "avg"),   # division by 5
+    ((1000, 37, 4096, 3, 129, 0, 8191), 8, "flat", 8, "bf16", "avg"),
+    ((1000, 37, 4096, 3, 129, 0, 8191), 1, "flat", 16, "fp16", "avg"),
+    ((1000, 37, 4096, 3, 129, 0, 8191), 16, "flat", 16, "bf16", "avg"),  # generic-N path
+    ((1000, 37, 4096, 3, 129, 0, 8191), 6, "round_robin", 1, "fp16", "sum"),
+    ((1000, 37, 4096, 3, 129, 0, 8191), 9, "round_robin", 1, "bf16", "avg"),  # empty shards
+    ((70001,), 7, "flat", 1, "fp16", "sum"),                             # one ragged tensor
+    ((1,), 4, "flat", 16, "bf16", "avg"),                                # one element
+    ((5, 3), 2, "round_robin", 1, "fp16", "avg"),
+]
+
+
+@pytest.mark.parametrize("numel,N,mode,A,dtype,op", SMALL)
+def test_small_groups(numel, N, mode, A, dtype, op):
+    w = W.small(numel, N, mode=mode, align=A, dtype=dtype, op=op, outlier_frac=0.01)
+    _run_full(w, 3)
+
+
+@pytest.mark.parametrize("hp", [Z.AdamW(lr=3e-2, beta1=0.8, beta2=0.95, eps=1e-6, weight_decay=0.1),
+                                Z.AdamW(lr=1e-4, weight_decay=0.0)], ids=["aggressive", "wd0"])
+def test_other_hyperparameters(hp):
+    w = W.small((3000, 17, 555), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    _run_full(w, 4, hp=hp)
+
+
+def test_large_step_count():
+    """Bias-correction constants at t = 1000 (beta2^t far from 1)."""
+    w = W.small((4096, 100), 2, mode="flat", align=16, dtype="fp16", op="avg")
+    c = Case(w)
+    for t in (999, 1000):
+        g = c.grads(t)
+        Z.zero_step(c.plan, g, w.op, c.master, c.m, c.v, c.full16, None, HP, t)
+        c.oracle_step(g, t, hp_oracle(HP))
+    torch.cuda.synchronize()
+    c.compare("t=1000")
+
+
+def test_non_default_stream():
+    w = W.small((5000, 33), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = _run_full(w, 2, stream=s)
+    assert c is not None
+
+
+def test_init_shards_exact():
+    w = W.small((1000, 37, 4096, 3), 3, mode="flat", align=2, dtype="bf16")
+    c = Case(w)
+    torch.cuda.synchronize()
+    for r in range(w.n_ranks):
+        assert np.array_equal(f32(c.master[r]).view(np.uint32), c.o_master[r].view(np.uint32))
+        assert not f32(c.m[r]).any() and not f32(c.v[r]).any()
+
+
+@pytest.mark.parametrize("bucket", [1, 7, 1000, 4096, 50_000])
+def test_results_do_not_depend_on_buckets(bucket):
+    w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    ref = Case(w, with_oracle=False)
+    got = Case(w, with_oracle=False)
+    for t in (1, 2):
+        g = ref.grads(t)
+        Z.zero_step(ref.plan, g, "avg", ref.master, ref.m, ref.v, ref.full16, None, HP, t)
+        Z.zero_step(got.plan, g, "avg", got.master, got.m, got.v, got.full16, None, HP, t,
+                    bucket_elems=bucket)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(ref.master[r], got.master[r])
+        assert torch.equal(ref.m[r], got.m[r]) and torch.equal(ref.v[r], got.v[r])
+    assert torch.equal(ref.full16, got.full16)
+
+
+@pytest.mark.parametrize("mode,N,A", [("flat", 4, 16), ("round_robin", 4, 1), ("flat", 3, 2)])
+def test_unfused_composition_is_bit_identical(mode, N, A):
+    """reduce_scatter -> adamw_shard_step -> allgather == zero_step, and the
+    pieces match the oracle's own unfused pieces."""
+    w = W.small((20000, 37, 4096, 3, 129), N, mode=mode, align=A, dtype="fp16", op="avg")
+    fused = Case(w, with_oracle=False)
+    parts = Case(w, with_oracle=False)
+    gsh = [torch.empty(parts.plan.shard_len(r), dtype=torch.float32, device="cuda")
+           for r in range(N)]
+    s16 = [torch.empty(parts.plan.shard_len(r), dtype=w.torch_dtype, device="cuda")
+           for r in range(N)]
+    for t in (1, 2):
+        g = fused.grads(t)
+        Z.zero_step(fused.plan, g, "avg", fused.master, fused.m, fused.v, fused.full16, None, HP, t)
+        Z.zero_reduce_scatter(parts.plan, g, "avg", gsh)
+        if t == 1:
+            torch.cuda.synchronize()
+            orc = [np.zeros(parts.plan.shard_len(r), np.float32) for r in range(N)]
+            oracle.reduce_scatter(list(w.numel), N, oracle.FLAT if mode == "flat" else
+                                  oracle.ROUND_ROBIN, A, dt_code(w), oracle.AVG,
+                                  [u16(x) for x in g], orc)
+            for r in range(N):
+                assert np.array_equal(f32(gsh[r]).view(np.uint32), orc[r].view(np.uint32))
+        Z.zero_adamw_shard_step(parts.plan, parts.master, parts.m, parts.v, gsh, s16, HP, t)
+        Z.zero_allgather(parts.plan, s16, parts.full16)
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert torch.equal(fused.master[r], parts.master[r])
+        assert torch.equal(fused.m[r], parts.m[r]) and torch.equal(fused.v[r], parts.v[r])
+    assert torch.equal(fused.full16, parts.full16)
+
+
+def test_rank_mask_touches_only_masked_ranks():
+    w = W.small((5000, 37, 4096), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    c = Case(w)
+    sentinel = float("nan")
+    for r in (1, 3):
+        c.master[r].fill_(sentinel)
+        c.m[r].fill_(sentinel)
+        c.v[r].fill_(sentinel)
+    c.full16.fill_(7)
+    before_full = u16(c.full16)
+    g = c.grads(1)
+    Z.zero_step(c.plan, g, "avg", c.master, c.m, c.v, c.full16, None, HP, 1, rank_mask=0b0101)
+    c.oracle_step(g, 1, hp_oracle(HP), mask=0b0101)
+    torch.cuda.synchronize()
+    for r in (1, 3):
+        assert torch.isnan(c.master[r]).all() and torch.isnan(c.v[r]).all()
+    full = u16(c.full16)
+    for r in (0, 2):
+        off, ln = c.plan.shards[r]
+        assert_16_close(full[off:off + ln], c.o_full[off:off + ln], f"full16 rank {r}")
+        assert_fp32_close(f32(c.master[r]), c.o_master[r], f"master[{r}]")
+    for r in (1, 3):
+        off, ln = c.plan.shards[r]
+        assert np.array_equal(full[off:off + ln], before_full[off:off + ln])
+
+
+def test_zero3_shard_output():
+    """out16_shard receives each rank's 16-bit shard, equal to its slot of
+    the gathered buffer."""
+    w = W.small((20000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    c = Case(w)
+    s16 = [torch.empty(c.plan.shard_len(r), dtype=w.torch_dtype, device="cuda") for r in range(4)]
+    g = c.grads(1)
+    Z.zero_step(c.plan, g, "avg", c.master, c.m, c.v, c.full16, s16, HP, 1)
+    c.oracle_step(g, 1, hp_oracle(HP))
+    torch.cuda.synchronize()
+    c.compare("zero3")
+    for r in range(4):
+        off, ln = c.plan.shards[r]
+        assert torch.equal(s16[r], c.full16[off:off + ln])
+
+
+# ----------------------------------------------------------------------------
+# full-size groups, sampled parity
+
+
+def _sampled(w: W.Workload, steps: int, hp=HP, n_random=20000):
+    """Run the CUDA step at full size and check sampled elements against the
+    oracle recomputing those elements one by one from the same inputs."""
+    extra = []
+    if w.bucket_elems:
+        extra = list(range(0, W.flat_len(w), w.bucket_elems))
+    F = sample_indices(w, n_random=n_random, extra=extra)
+    rank, shard = owner_of(w, F)
+    keep = np.array([(w.mask >> int(r)) & 1 for r in rank], bool) & (rank >= 0)
+    F, rank, shard = F[keep], rank[keep], shard[keep]
+    Ft = torch.from_numpy(F).cuda()
+    c = Case(w, with_oracle=False)
+    ext = c.plan.flat_extent(w.mask)
+    dt, op = dt_code(w), op_code(w)
+    om = oracle.to_f32(u16(c.p16[Ft]), dt)
+    mm, vv = np.zeros_like(om), np.zeros_like(om)
+    out = np.zeros(F.size, np.uint16)
+    for t in range(1, steps + 1):
+        g = [W.grads16(w, t, q, "cuda", 0, ext) for q in range(w.n_ranks)]
+        gs = np.stack([u16(x[Ft]) for x in g])
+        Z.zero_step(c.plan, g, w.op, c.master, c.m, c.v, c.full16[:ext], None, hp, t,
+                    rank_mask=w.mask, bucket_elems=w.bucket_elems)
+        oracle.update_elements(gs, om, mm, vv, dt, op, hp_oracle(hp), t, out16=out)
+        del g
+    torch.cuda.synchronize()
+    got_p = np.empty(F.size, np.float32)
+    got_m = np.empty(F.size, np.float32)
+    got_v = np.empty(F.size, np.float32)
+    for r in np.unique(rank):
+        sel = rank == r
+        it = torch.from_numpy(shard[sel]).cuda()
+        got_p[sel] = f32(c.master[r][it])
+        got_m[sel] = f32(c.m[r][it])
+        got_v[sel] = f32(c.v[r][it])
+    assert_fp32_close(got_p, om, f"{w.key} master")
+    assert_fp32_close(got_m, mm, f"{w.key} m")
+    assert_fp32_close(got_v, vv, f"{w.key} v")
+    assert_16_close(u16(c.full16[Ft]), out, f"{w.key} full16")
+    return F.size
+
+
+def test_bert_base_full_size_sampled():
+    assert _sampled(W.WORKLOADS["bert_base"], 10) > 20000
+
+
+def test_toy_model_round_robin_full_size_sampled():
+    assert _sampled(W.WORKLOADS["toy_rr"], 3) > 20000
+
+
+def test_llama7b_rank0_shard_full_size_sampled():
+    """Rank 0's 842M-element shard, 8 bf16 gradient slices, 50M-element
+    buckets (the gradient buffers hold only rank 0's flat range)."""
+    assert _sampled(W.WORKLOADS["llama7b_rank0"], 3, n_random=8000) > 8000
+
+
+def test_llama13b_zero3_layer_pass_sampled():
+    """Two layers of the ZeRO-3 stream: all-gather 8 bf16 shards into the
+    layer buffer (bit-exact), then the fused step writing each rank's shard."""
+    w = W.WORKLOADS["llama13b_layer"]
+    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+    L = W.flat_len(w)
+    S = plan.shard_len(0)
+    layer_buf = torch.empty(L, dtype=w.torch_dtype, device="cuda")
+    F = sample_indices(w, n_random=8000)
+    rank, shard = owner_of(w, F)
+    Ft = torch.from_numpy(F).cuda()
+    dt, op = dt_code(w), op_code(w)
+    for layer in range(2):
+        p16 = W.params16(w, "cuda", layer=layer)
+        shards = [p16[r * S:(r + 1) * S].clone() for r in range(w.n_ranks)]
+        master = [torch.empty(S, dtype=torch.float32, device="cuda") for _ in range(w.n_ranks)]
+        m = [torch.empty_like(x) for x in master]
+        v = [torch.empty_like(x) for x in master]
+        Z.zero_init_shards(plan, p16, master, m, v)
+        Z.zero_allgather(plan, shards, layer_buf)
+        torch.cuda.synchronize()
+        assert torch.equal(layer_buf, p16)
+        om = oracle.to_f32(u16(p16[Ft]), dt)
+        mm, vv = np.zeros_like(om), np.zeros_like(om)
+        out = np.zeros(F.size, np.uint16)
+        g = [W.grads16(w, 1, q, "cuda", layer=layer) for q in range(w.n_ranks)]
+        gs = np.stack([u16(x[Ft]) for x in g])
+        Z.zero_step(plan, g, "avg", master, m, v, None, shards, HP, 1)
+        oracle.update_elements(gs, om, mm, vv, dt, op, hp_oracle(HP), 1, out16=out)
+        torch.cuda.synchronize()
+        for r in range(w.n_ranks):
+            sel = rank == r
+            it = torch.from_numpy(shard[sel]).cuda()
+            assert_fp32_close(f32(master[r][it]), om[sel], f"layer {layer} master[{r}]")
+            assert_fp32_close(f32(m[r][it]), mm[sel], f"layer {layer} m[{r}]")
+            assert_fp32_close(f32(v[r][it]), vv[sel], f"layer {layer} v[{r}]")
+            assert_16_close(u16(shards[r][it]), out[sel], f"layer {layer} shard16[{r}]")
+        # the next gather reproduces the updated shards in the layer buffer
+        Z.zero_allgather(plan, shards, layer_buf)
+        torch.cuda.synchronize()
+        assert torch.equal(layer_buf, torch.cat(shards))
+        del g, shards, master, m, v, p16

@@ -1,0 +1,359 @@
+// C-ABI device calls of the ZeRO sharded optimizer step: argument checks,
+// the per-step AdamW constants, the job tables and the launches.
+//
+// What each call computes is documented in include/zero.h; the sources are
+// "DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com) §4.1-§4.4 for
+// init / reduce-scatter / local update / all-gather, and "ZeRO 优化器"
+// (cookllm.com) 梯度同步 for the summed (rather than averaged) reduction.
+#include <cuda_runtime.h>
+#include <inttypes.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <new>
+#include <vector>
+
+#include "zero_capi_util.h"
+#include "zero_internal.h"
+
+namespace zero {
+
+char* error_buffer() {
+  static thread_local char buf[1024];
+  return buf;
+}
+
+std::atomic<int64_t> g_launches{0};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+zero_status check_plan_mask(const char* fn, const zero_plan* plan, uint64_t rank_mask) {
+  if (!plan) return fail(ZERO_ERR_INVALID, "%s: plan is NULL", fn);
+  if (rank_mask == 0) return fail(ZERO_ERR_INVALID, "%s: rank_mask selects no rank", fn);
+  if (plan->n_ranks < 64 && (rank_mask >> plan->n_ranks) != 0)
+    return fail(ZERO_ERR_INVALID, "%s: rank_mask 0x%" PRIx64 " names a rank >= n_ranks (%d)", fn,
+                rank_mask, plan->n_ranks);
+  return ZERO_OK;
+}
+
+bool in_mask(uint64_t mask, int r) { return (mask >> r) & 1u; }
+
+zero_status check_dtype(const char* fn, zero_dtype dtype) {
+  if (dtype != ZERO_FP16 && dtype != ZERO_BF16) return fail(ZERO_ERR_INVALID, "%s: unknown dtype", fn);
+  return ZERO_OK;
+}
+
+// Per-rank pointer array: every masked rank's entry non-NULL (unless
+// nullable) and 16-byte aligned.
+template <class P>
+zero_status check_ptrs(const char* fn, const char* what, P const* arr, const zero_plan* plan,
+                       uint64_t mask, bool nullable_entries, bool all_ranks = false) {
+  if (!arr) return fail(ZERO_ERR_INVALID, "%s: %s is NULL", fn, what);
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!all_ranks && !in_mask(mask, r)) continue;
+    if (!all_ranks && plan->shard_len[r] == 0) continue;  // an empty shard is never touched
+    const void* p = arr[r];
+    if (!p) {
+      if (nullable_entries) continue;
+      return fail(ZERO_ERR_INVALID, "%s: %s[%d] is NULL", fn, what, r);
+    }
+    if (!aligned16(p)) return fail(ZERO_ERR_ALIGN, "%s: %s[%d] is not 16-byte aligned", fn, what, r);
+  }
+  return ZERO_OK;
+}
+
+zero_status check_hparams(const char* fn, const zero_adamw_hparams* hp, int64_t step) {
+  if (!hp) return fail(ZERO_ERR_INVALID, "%s: hparams is NULL", fn);
+  const double vals[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  for (double x : vals)
+    if (!isfinite(x)) return fail(ZERO_ERR_INVALID, "%s: non-finite hyper-parameter", fn);
+  if (hp->lr < 0 || hp->weight_decay < 0 || !(hp->eps > 0))
+    return fail(ZERO_ERR_INVALID, "%s: need lr >= 0, weight_decay >= 0, eps > 0", fn);
+  if (hp->beta1 < 0 || hp->beta1 >= 1 || hp->beta2 < 0 || hp->beta2 >= 1)
+    return fail(ZERO_ERR_INVALID, "%s: betas must lie in [0, 1)", fn);
+  if (step < 1) return fail(ZERO_ERR_INVALID, "%s: step must be >= 1 (got %" PRId64 ")", fn, step);
+  return ZERO_OK;
+}
+
+// The binary32 constants of step t, each formed in binary64 and rounded once.
+StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t) {
+  StepScalars s;
+  s.d = static_cast<float>(1.0 - h.lr * h.weight_decay);
+  s.b1 = static_cast<float>(h.beta1);
+  s.b2 = static_cast<float>(h.beta2);
+  s.c1 = static_cast<float>(1.0 - h.beta1);
+  s.c2 = static_cast<float>(1.0 - h.beta2);
+  s.ss = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
+  s.sb = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
+  s.eps = static_cast<float>(h.eps);
+  return s;
+}
+
+void set_scale(LaunchArgs& a, int n_ranks, zero_reduce_op op) {
+  a.n_ranks = n_ranks;
+  a.n_f = static_cast<float>(n_ranks);
+  a.inv_n = 1.0f / static_cast<float>(n_ranks);
+  if (op == ZERO_REDUCE_SUM || n_ranks == 1)
+    a.scale_mode = kScaleNone;
+  else if ((n_ranks & (n_ranks - 1)) == 0)
+    a.scale_mode = kScaleMul;  // 1/N exact
+  else
+    a.scale_mode = kScaleDiv;
+}
+
+// Split one run into vector and element-wise jobs.
+void add_run(std::vector<Job>& out, int r, int64_t flat, int64_t shard, int64_t len) {
+  if (len <= 0) return;
+  if ((flat - shard) % kVec != 0) {  // flat and shard never co-aligned
+    out.push_back({flat, shard, len, 0, r, 0});
+    return;
+  }
+  int64_t head = (kVec - flat % kVec) % kVec;
+  if (head > len) head = len;
+  if (head) out.push_back({flat, shard, head, 0, r, 0});
+  const int64_t body = (len - head) / kVec * kVec;
+  if (body) out.push_back({flat + head, shard + head, body, 0, r, 1});
+  const int64_t tail = len - head - body;
+  if (tail) out.push_back({flat + head + body, shard + head + body, tail, 0, r, 0});
+}
+
+// Jobs of the masked ranks restricted to the flat range [lo, hi).
+void build_jobs(const zero_plan* plan, uint64_t mask, int64_t lo, int64_t hi,
+                std::vector<Job>& jobs) {
+  jobs.clear();
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!in_mask(mask, r)) continue;
+    for (const auto& run : plan->runs[r]) {
+      const int64_t a = std::max(lo, run.flat_off);
+      const int64_t b = std::min(hi, run.flat_off + run.len);
+      if (a < b) add_run(jobs, r, a, run.shard_off + (a - run.flat_off), b - a);
+    }
+  }
+}
+
+// Launch `kind` over `jobs`, at most kMaxJobs per launch.
+zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs& a,
+                        const std::vector<Job>& jobs, void* stream) {
+  size_t j0 = 0;
+  while (j0 < jobs.size()) {
+    const size_t nj = std::min<size_t>(jobs.size() - j0, kMaxJobs);
+    int64_t tiles = 0;
+    for (size_t j = 0; j < nj; ++j) {
+      a.jobs[j] = jobs[j0 + j];
+      a.jobs[j].tile_begin = tiles;
+      tiles += (a.jobs[j].len + kTile - 1) / kTile;
+    }
+    a.n_jobs = static_cast<int32_t>(nj);
+    a.n_tiles = tiles;
+    const int err = launch_kernel(kind, dtype, a, stream);
+    if (err != 0)
+      return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
+                  cudaGetErrorString(static_cast<cudaError_t>(err)));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    j0 += nj;
+  }
+  return ZERO_OK;
+}
+
+// Run `kind` bucket by bucket over the flat index space.
+zero_status run_buckets(const char* fn, Kind kind, zero_dtype dtype, const zero_plan* plan,
+                        uint64_t mask, int64_t bucket, LaunchArgs& a, void* stream) {
+  std::vector<Job> jobs;
+  const int64_t total = plan->padded;
+  const int64_t B = bucket > 0 ? bucket : std::max<int64_t>(total, 1);
+  // Only buckets that meet a masked rank's run launch anything.
+  for (int64_t lo = 0; lo < total; lo += B) {
+    const int64_t hi = std::min(total, lo + B);
+    build_jobs(plan, mask, lo, hi, jobs);
+    if (jobs.empty()) continue;
+    const zero_status st = launch_jobs(fn, kind, dtype, a, jobs, stream);
+    if (st != ZERO_OK) return st;
+  }
+  return ZERO_OK;
+}
+
+zero_status pending_error(const char* fn) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(ZERO_ERR_CUDA, "%s: pending CUDA error: %s", fn, cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
+LaunchArgs* new_args() {
+  LaunchArgs* a = new (std::nothrow) LaunchArgs;
+  if (a) memset(a, 0, sizeof(LaunchArgs));
+  return a;
+}
+
+struct ArgsHolder {
+  LaunchArgs* p;
+  explicit ArgsHolder(LaunchArgs* q) : p(q) {}
+  ~ArgsHolder() { delete p; }
+};
+
+}  // namespace
+}  // namespace zero
+
+using namespace zero;
+
+#define ZERO_TRY(x)                    \
+  do {                                 \
+    const zero_status st_ = (x);       \
+    if (st_ != ZERO_OK) return st_;    \
+  } while (0)
+
+extern "C" zero_status zero_init_shards(const zero_plan* plan, const void* full_flat16,
+                                        zero_dtype dtype, float* const* master, float* const* m,
+                                        float* const* v, uint64_t rank_mask, void* stream) {
+  const char* fn = "zero_init_shards";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (!full_flat16) return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
+  if (!aligned16(full_flat16)) return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!in_mask(rank_mask, r)) continue;
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+  }
+  a.full16 = const_cast<void*>(full_flat16);
+  return run_buckets(fn, Kind::kInit, dtype, plan, rank_mask, 0, a, stream);
+}
+
+extern "C" zero_status zero_reduce_scatter(const zero_plan* plan, const void* const* grads,
+                                           zero_dtype dtype, zero_reduce_op op,
+                                           float* const* grad_shards, uint64_t rank_mask,
+                                           int64_t bucket_elems, void* stream) {
+  const char* fn = "zero_reduce_scatter";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (in_mask(rank_mask, r)) a.gshard[r] = grad_shards[r];
+  }
+  set_scale(a, plan->n_ranks, op);
+  return run_buckets(fn, Kind::kReduceScatter, dtype, plan, rank_mask, bucket_elems, a, stream);
+}
+
+extern "C" zero_status zero_adamw_shard_step(const zero_plan* plan, float* const* master,
+                                             float* const* m, float* const* v,
+                                             const float* const* grad_shards,
+                                             void* const* out16_shard, zero_dtype dtype,
+                                             const zero_adamw_hparams* hp, int64_t step,
+                                             uint64_t rank_mask, void* stream) {
+  const char* fn = "zero_adamw_shard_step";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  ZERO_TRY(check_hparams(fn, hp, step));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  if (out16_shard) ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, true));
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!in_mask(rank_mask, r)) continue;
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+    a.gshard[r] = const_cast<float*>(grad_shards[r]);
+    a.shard16[r] = out16_shard ? out16_shard[r] : nullptr;
+  }
+  a.sc = make_scalars(*hp, step);
+  return run_buckets(fn, Kind::kAdamw, dtype, plan, rank_mask, 0, a, stream);
+}
+
+extern "C" zero_status zero_allgather(const zero_plan* plan, const void* const* shards16,
+                                      zero_dtype dtype, void* full_flat16, uint64_t rank_mask,
+                                      void* stream) {
+  const char* fn = "zero_allgather";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  ZERO_TRY(check_ptrs(fn, "shards16", shards16, plan, rank_mask, false));
+  if (!full_flat16) return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
+  if (!aligned16(full_flat16)) return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r)
+    if (in_mask(rank_mask, r)) a.shard16[r] = const_cast<void*>(shards16[r]);
+  a.full16 = full_flat16;
+  return run_buckets(fn, Kind::kAllgather, dtype, plan, rank_mask, 0, a, stream);
+}
+
+extern "C" zero_status zero_step(const zero_plan* plan, const void* const* grads,
+                                 zero_dtype dtype, zero_reduce_op op, float* const* master,
+                                 float* const* m, float* const* v, void* full_flat16,
+                                 void* const* out16_shard, const zero_adamw_hparams* hp,
+                                 int64_t step, uint64_t rank_mask, int64_t bucket_elems,
+                                 void* stream) {
+  const char* fn = "zero_step";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, step));
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  if (out16_shard) ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, true));
+  if (full_flat16 && !aligned16(full_flat16))
+    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (!in_mask(rank_mask, r)) continue;
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+    a.shard16[r] = out16_shard ? out16_shard[r] : nullptr;
+  }
+  a.full16 = full_flat16;
+  a.sc = make_scalars(*hp, step);
+  set_scale(a, plan->n_ranks, op);
+  return run_buckets(fn, Kind::kStep, dtype, plan, rank_mask, bucket_elems, a, stream);
+}
+
+extern "C" zero_status zero_sync(void* stream) {
+  clear_error();
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ZERO_ERR_CUDA, "zero_sync: %s", cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
+extern "C" const char* zero_last_error(void) { return error_buffer(); }
+
+extern "C" int64_t zero_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char* zero_version(void) { return "zero-gb300 0.1.0 (sm_103a)"; }

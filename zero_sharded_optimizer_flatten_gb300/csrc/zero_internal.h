@@ -1,0 +1,93 @@
+// Internal structures shared by the host launcher and the CUDA kernels of the
+// ZeRO sharded optimizer step.  Not part of the public ABI (include/zero.h).
+#pragma once
+
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "zero.h"
+
+namespace zero {
+
+constexpr int kMaxRanks = 64;     // rank_mask is a uint64_t
+constexpr int kThreads = 256;     // threads per CTA of every kernel
+constexpr int kVec = 8;           // 16-bit elements per 16-byte vector
+constexpr int kTile = kThreads * kVec;  // elements one CTA covers per tile
+constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
+
+// Binary32 constants of one AdamW step, formed on the host in binary64 and
+// rounded once each (see zero_adamw_hparams).
+struct StepScalars {
+  float d, b1, b2, c1, c2, ss, sb, eps;
+};
+
+// How the rank-ordered sum becomes the gradient: kept (SUM), multiplied by the
+// exact power of two 1/N, or divided by N.  Multiplying by an exact 1/N and
+// dividing by N round the same real number, so both give the binary32
+// quotient of the sum by N.
+enum ScaleMode : int32_t { kScaleNone = 0, kScaleMul = 1, kScaleDiv = 2 };
+
+// A contiguous run of one rank's elements: flat indices
+// [flat_off, flat_off + len) map to shard indices [shard_off, shard_off + len).
+// vec != 0: flat_off, shard_off and len are multiples of kVec, so the run is
+// processed in 16-byte vectors; otherwise element by element.
+struct Job {
+  int64_t flat_off;
+  int64_t shard_off;
+  int64_t len;
+  int64_t tile_begin;  // index of the job's first tile in the launch
+  int32_t rank;
+  int32_t vec;
+};
+
+// Parameters of one launch.  Passed by value as a __grid_constant__ kernel
+// parameter (about 10 KB), so the job table needs no device allocation.
+struct LaunchArgs {
+  const void* grads[kMaxRanks];  // 16-bit flat replicas (reduce/step)
+  float* master[kMaxRanks];
+  float* m[kMaxRanks];
+  float* v[kMaxRanks];
+  float* gshard[kMaxRanks];        // fp32 reduced gradient shards (adamw in / reduce out)
+  void* shard16[kMaxRanks];        // 16-bit shard buffers (nullable entries)
+  void* full16;                    // gathered flat 16-bit buffer (nullable)
+  StepScalars sc;
+  float inv_n;                     // 1/N when N is a power of two
+  float n_f;                       // N as binary32
+  int32_t scale_mode;
+  int32_t n_ranks;                 // gradient replicas summed
+  int32_t n_jobs;
+  int32_t pad_;
+  int64_t n_tiles;
+  Job jobs[kMaxJobs];
+};
+
+enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit };
+
+// Host launcher entry (zero_kernels_*.cu): launches `kind` for the jobs in
+// `a` on `stream`; returns a CUDA error code (0 on success).
+int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream);
+
+}  // namespace zero
+
+// The plan: the library's own description of one parameter group.
+struct zero_plan {
+  int32_t n_ranks = 0;
+  int32_t mode = 0;
+  int32_t align = 1;
+  int64_t phi = 0;      // real elements
+  int64_t padded = 0;   // length of the gathered flat buffer
+  std::vector<int64_t> numel;
+  std::vector<int64_t> tensor_start;  // flat index of each tensor's first element
+  std::vector<int64_t> shard_len;     // per rank
+  std::vector<int64_t> shard_flat;    // per rank: flat index of the shard (flat mode) or -1
+  struct Seg {
+    int64_t tensor, tensor_off, flat_off, shard_off, len;
+  };
+  std::vector<std::vector<Seg>> segs;  // per rank, increasing flat order
+  struct Run {
+    int64_t flat_off, shard_off, len;
+  };
+  std::vector<std::vector<Run>> runs;  // per rank: maximal runs contiguous in both spaces
+};

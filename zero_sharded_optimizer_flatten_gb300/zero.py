@@ -1,0 +1,407 @@
+"""Python binding of the C ABI in include/zero.h (ctypes; argument marshalling only).
+
+Every function keeps the C name and forwards to libzero.so.  Tensors are
+torch tensors on the GPU (or raw integer device addresses); the binding only
+checks dtypes, devices, contiguity and sizes against the plan, turns them into
+pointer arrays and passes the current CUDA stream.  There is no fallback: if
+libzero.so is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzero.so")
+
+ZERO_OK, ZERO_ERR_INVALID, ZERO_ERR_ALIGN, ZERO_ERR_CUDA, ZERO_ERR_OOM = 0, 1, 2, 3, 4
+ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED = 5, 6
+ZERO_FP16, ZERO_BF16 = 0, 1
+ZERO_PART_FLAT, ZERO_PART_ROUND_ROBIN = 0, 1
+ZERO_REDUCE_SUM, ZERO_REDUCE_AVG = 0, 1
+
+_MODES = {"flat": ZERO_PART_FLAT, "round_robin": ZERO_PART_ROUND_ROBIN}
+_OPS = {"sum": ZERO_REDUCE_SUM, "avg": ZERO_REDUCE_AVG}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[status {status}] {message}")
+        self.status = status
+
+
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double)]
+
+
+@dataclasses.dataclass
+class AdamW:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+
+    def c(self) -> AdamWHparams:
+        return AdamWHparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay)
+
+
+def lib():
+    """Load libzero.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; "
+                    "g.build()'` (needs nvcc); there is no fallback implementation")
+            L = ctypes.CDLL(LIB_PATH)
+            i64, i32, u64, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p
+            i64p, i32p = ctypes.POINTER(i64), ctypes.POINTER(i32)
+            vpp = ctypes.POINTER(vp)
+            hp = ctypes.POINTER(AdamWHparams)
+            sig = {
+                "zero_plan_partitions": [i64p, i32, i32, ctypes.c_int, i32,
+                                         ctypes.POINTER(vp)],
+                "zero_plan_total": [vp, i64p, i64p],
+                "zero_plan_info": [vp, i32p, i32p, i32p, i32p],
+                "zero_plan_shard": [vp, i32, i64p, i64p],
+                "zero_plan_segments": [vp, i32, i64p, i64p, i64p, i64p, i64p, i64, i64p],
+                "zero_plan_describe": [vp, ctypes.c_char_p, i64],
+                "zero_memory_bytes": [i32, i64, i32, i64p, i64p],
+                "zero_init_shards": [vp, vp, ctypes.c_int, vpp, vpp, vpp, u64, vp],
+                "zero_reduce_scatter": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, u64, i64, vp],
+                "zero_adamw_shard_step": [vp, vpp, vpp, vpp, vpp, vpp, ctypes.c_int, hp, i64,
+                                          u64, vp],
+                "zero_allgather": [vp, vpp, ctypes.c_int, vp, u64, vp],
+                "zero_step": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vp, vpp, hp,
+                              i64, u64, i64, vp],
+                "zero_sync": [vp],
+            }
+            for name, args in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.zero_plan_destroy.argtypes = [vp]
+            L.zero_plan_destroy.restype = None
+            L.zero_last_error.restype = ctypes.c_char_p
+            L.zero_version.restype = ctypes.c_char_p
+            L.zero_launch_count.restype = i64
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != ZERO_OK:
+        raise ZeroError(status, zero_last_error())
+
+
+def zero_last_error() -> str:
+    return lib().zero_last_error().decode()
+
+
+def zero_version() -> str:
+    return lib().zero_version().decode()
+
+
+def zero_launch_count() -> int:
+    return int(lib().zero_launch_count())
+
+
+# ----------------------------------------------------------------------------
+# plan
+
+
+class Plan:
+    """Owner of a zero_plan* (released when garbage-collected)."""
+
+    def __init__(self, handle: int, numel):
+        self._h = ctypes.c_void_p(handle)
+        self.numel = tuple(int(x) for x in numel)
+        n, mode, align, nt = (ctypes.c_int32() for _ in range(4))
+        _check(lib().zero_plan_info(self._h, ctypes.byref(n), ctypes.byref(mode),
+                                    ctypes.byref(align), ctypes.byref(nt)))
+        self.n_ranks, self.mode, self.align = n.value, mode.value, align.value
+        phi, padded = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().zero_plan_total(self._h, ctypes.byref(phi), ctypes.byref(padded)))
+        self.phi, self.padded = phi.value, padded.value
+        self.shards = [self._shard(r) for r in range(self.n_ranks)]
+        self._seg_cache = {}
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.zero_plan_destroy(h)
+            self._h = None
+
+    def _shard(self, r):
+        off, ln = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().zero_plan_shard(self._h, r, ctypes.byref(off), ctypes.byref(ln)))
+        return off.value, ln.value
+
+    def shard_len(self, r: int) -> int:
+        return self.shards[r][1]
+
+    def segments(self, r: int) -> np.ndarray:
+        """Rows (tensor_idx, tensor_off, flat_off, shard_off, len) of rank r."""
+        if r in self._seg_cache:
+            return self._seg_cache[r]
+        n = ctypes.c_int64()
+        _check(lib().zero_plan_segments(self._h, r, None, None, None, None, None, 0,
+                                        ctypes.byref(n)))
+        out = np.zeros((5, max(1, n.value)), np.int64)
+        ptrs = [out[i].ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) for i in range(5)]
+        _check(lib().zero_plan_segments(self._h, r, *ptrs, n.value, ctypes.byref(n)))
+        seg = out[:, :n.value].T.copy()
+        self._seg_cache[r] = seg
+        return seg
+
+    def flat_extent(self, mask: int) -> int:
+        """One past the largest flat index owned by a rank in mask."""
+        ext = 0
+        for r in range(self.n_ranks):
+            if (mask >> r) & 1:
+                seg = self.segments(r)
+                if len(seg):
+                    ext = max(ext, int((seg[:, 2] + seg[:, 4]).max()))
+        return ext
+
+    def describe(self) -> str:
+        buf = ctypes.create_string_buffer(1 << 16)
+        _check(lib().zero_plan_describe(self._h, buf, len(buf)))
+        return buf.value.decode()
+
+    @property
+    def all_ranks(self) -> int:
+        return (1 << self.n_ranks) - 1
+
+
+def zero_plan_partitions(numel: Sequence[int], n_ranks: int, mode="flat",
+                         align_elems: int = 16) -> Plan:
+    arr = (ctypes.c_int64 * max(1, len(numel)))(*[int(x) for x in numel])
+    mode_i = _MODES[mode] if isinstance(mode, str) else int(mode)
+    out = ctypes.c_void_p()
+    _check(lib().zero_plan_partitions(arr, len(numel), n_ranks, mode_i, align_elems,
+                                      ctypes.byref(out)))
+    return Plan(out.value, numel)
+
+
+def zero_memory_bytes(stage: int, phi: int, n_ranks: int):
+    num, den = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zero_memory_bytes(stage, phi, n_ranks, ctypes.byref(num), ctypes.byref(den)))
+    return num.value, den.value
+
+
+# ----------------------------------------------------------------------------
+# marshalling
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ZERO_FP16
+    if t.dtype == torch.bfloat16:
+        return ZERO_BF16
+    raise TypeError(f"expected a float16 or bfloat16 tensor, got {t.dtype}")
+
+
+def _addr(t, what: str, min_numel: Optional[int] = None, dtype=None) -> int:
+    """Device address of a tensor (or pass-through of an int address)."""
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch.Tensor or an int address")
+    if not t.is_cuda:
+        raise ValueError(f"{what}: tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{what}: has {t.numel()} elements, needs at least {min_numel}")
+    return t.data_ptr()
+
+
+def _ptrs(values):
+    return (ctypes.c_void_p * max(1, len(values)))(*[v or None for v in values])
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        torch = _torch()
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _mask(plan: Plan, rank_mask) -> int:
+    return plan.all_ranks if rank_mask is None else int(rank_mask)
+
+
+def _per_rank(plan, seq, what, mask, dtype=None, nullable=False, sized=True):
+    if seq is None:
+        raise ValueError(f"{what}: a list of {plan.n_ranks} entries is required")
+    if len(seq) != plan.n_ranks:
+        raise ValueError(f"{what}: expected {plan.n_ranks} entries, got {len(seq)}")
+    out = []
+    for r, t in enumerate(seq):
+        if not (mask >> r) & 1:
+            out.append(0)
+            continue
+        if t is None and nullable:
+            out.append(0)
+            continue
+        if t is None:
+            raise ValueError(f"{what}[{r}] is None for a masked rank")
+        out.append(_addr(t, f"{what}[{r}]", plan.shard_len(r) if sized else None, dtype))
+    return out
+
+
+def _sixteen(seq):
+    for t in seq:
+        if t is not None and not isinstance(t, int):
+            return _dtype_code(t)
+    raise ValueError("cannot infer the 16-bit dtype: pass dtype=")
+
+
+# ----------------------------------------------------------------------------
+# device calls
+
+
+def zero_init_shards(plan: Plan, full_flat16, master, m, v, rank_mask=None, stream=None,
+                     dtype=None):
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _dtype_code(full_flat16) if dtype is None else dtype
+    full = _addr(full_flat16, "full_flat16", plan.flat_extent(mask))
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    _check(lib().zero_init_shards(plan.handle, full, dt, _ptrs(ms), _ptrs(mm), _ptrs(vv), mask,
+                                  _stream(stream)))
+
+
+def zero_reduce_scatter(plan: Plan, grads, op, grad_shards, rank_mask=None, bucket_elems=0,
+                        stream=None, dtype=None):
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    out = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    _check(lib().zero_reduce_scatter(plan.handle, _ptrs(g), dt, op_i, _ptrs(out), mask,
+                                     int(bucket_elems), _stream(stream)))
+
+
+def zero_adamw_shard_step(plan: Plan, master, m, v, grad_shards, out16_shard, hparams: AdamW,
+                          step: int, rank_mask=None, stream=None, dtype=None):
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    if out16_shard is not None:
+        dt = _sixteen(out16_shard) if dtype is None else dtype
+        o16 = _ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+    else:
+        if dtype is None:
+            raise ValueError("dtype is required when out16_shard is None")
+        dt, o16 = dtype, None
+    hp = hparams.c()
+    _check(lib().zero_adamw_shard_step(plan.handle, _ptrs(ms), _ptrs(mm), _ptrs(vv), _ptrs(gs),
+                                       o16, dt, ctypes.byref(hp), int(step), mask,
+                                       _stream(stream)))
+
+
+def zero_allgather(plan: Plan, shards16, full_flat16, rank_mask=None, stream=None, dtype=None):
+    mask = _mask(plan, rank_mask)
+    dt = _dtype_code(full_flat16) if dtype is None else dtype
+    sh = _per_rank(plan, shards16, "shards16", mask)
+    full = _addr(full_flat16, "full_flat16", plan.flat_extent(mask))
+    _check(lib().zero_allgather(plan.handle, _ptrs(sh), dt, full, mask, _stream(stream)))
+
+
+def zero_step(plan: Plan, grads, op, master, m, v, full_flat16, out16_shard, hparams: AdamW,
+              step: int, rank_mask=None, bucket_elems=0, stream=None, dtype=None):
+    """The fused reduce-scatter + AdamW + cast + all-gather (see zero.h)."""
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    o16 = (_ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+           if out16_shard is not None else None)
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    hp = hparams.c()
+    _check(lib().zero_step(plan.handle, _ptrs(g), dt, op_i, _ptrs(ms), _ptrs(mm), _ptrs(vv),
+                           full, o16, ctypes.byref(hp), int(step), mask, int(bucket_elems),
+                           _stream(stream)))
+
+
+def zero_sync(stream=None):
+    _check(lib().zero_sync(_stream(stream)))
+
+
+class ZeroStep:
+    """A prepared fused step: the pointer arrays of one set of buffers are
+    marshalled once, and each call passes them straight to zero_step.  Used
+    where per-call Python overhead would show next to the kernel (benchmark
+    loops, the ZeRO-3 layer stream)."""
+
+    def __init__(self, plan: Plan, grads, op, master, m, v, full_flat16, out16_shard,
+                 hparams: AdamW, rank_mask=None, bucket_elems=0, dtype=None):
+        torch = _torch()
+        mask = _mask(plan, rank_mask)
+        self.plan, self.mask, self.bucket = plan, mask, int(bucket_elems)
+        self.dt = _sixteen(grads) if dtype is None else dtype
+        ext = plan.flat_extent(mask)
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        self._g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
+        self._ms = _ptrs(_per_rank(plan, master, "master", mask, torch.float32))
+        self._mm = _ptrs(_per_rank(plan, m, "m", mask, torch.float32))
+        self._vv = _ptrs(_per_rank(plan, v, "v", mask, torch.float32))
+        self._full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+        self._o16 = (_ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+                     if out16_shard is not None else None)
+        self.op = _OPS[op] if isinstance(op, str) else int(op)
+        self._hp = hparams.c()
+        self._keep = (grads, master, m, v, full_flat16, out16_shard)
+
+    def __call__(self, step: int, stream=None):
+        _check(lib().zero_step(self.plan.handle, self._g, self.dt, self.op, self._ms, self._mm,
+                               self._vv, self._full, self._o16, ctypes.byref(self._hp),
+                               int(step), self.mask, self.bucket, _stream(stream)))
