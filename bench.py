@@ -252,7 +252,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     from zero_sharded_optimizer_flatten_gb300 import workloads as W
-    w = W.WORKLOADS[WORKLOAD]
+    w = W.WORKLOADS[args.workload]
     rate, _ = oracle_rate(w, 1 << 16)
     total_budget = 60.0
     n = int(rate * total_budget / max(1, args.steps + args.warmup))
@@ -274,7 +274,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": W.WORKLOADS[WORKLOAD].title, "phi": w.phi,
+        "config": {"workload": w.title, "phi": w.phi,
                    "virtual_ranks": w.n_ranks, "sample_elements_per_step": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{n} of {w.phi} elements per step, single-threaded C oracle"},
@@ -294,7 +294,7 @@ def run_gpu(args, world, rank, local):
         raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
     torch.cuda.set_device(local)
     dist = init_dist(world, "nccl")
-    w = W.WORKLOADS[WORKLOAD]
+    w = W.WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
     P = plan.padded
@@ -307,7 +307,7 @@ def run_gpu(args, world, rank, local):
     m = [torch.empty_like(x) for x in master]
     v = [torch.empty_like(x) for x in master]
     Z.zero_init_shards(plan, p16, master, m, v)
-    n_sets = 2  # distinct gradient sets, alternated step to step
+    n_sets = args.grad_sets  # distinct gradient sets, alternated step to step
     grads = [[W.grads16(w, s + 1, q, dev) for q in range(w.n_ranks)] for s in range(n_sets)]
     steps = [Z.ZeroStep(plan, g, w.op, master, m, v, full16, None, hp) for g in grads]
     stream = torch.cuda.current_stream(dev)
@@ -408,7 +408,7 @@ def run_gpu(args, world, rank, local):
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": recorded_traffic(WORKLOAD),
+            "traffic": recorded_traffic(args.workload),
             "kernel": KERNEL_PREFIX,
             "bytes_per_launch": bytes_per_launch,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
@@ -442,6 +442,10 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="parameter group to time (the reported line uses the default)")
+    ap.add_argument("--grad-sets", type=int, default=2,
+                    help="distinct gradient sets resident in HBM, alternated per step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -148,7 +148,16 @@ def sample_indices(w: W.Workload, n_random: int = 20000, seed: int = 99, extra=(
     next to shard starts, and caller-given extras (bucket edges)."""
     L = W.flat_len(w)
     rng = np.random.default_rng(seed)
-    pts = [rng.integers(0, L, n_random)]
+    # random points inside the flat ranges of the masked ranks only
+    ranges = []
+    for r in range(w.n_ranks):
+        if (w.mask >> r) & 1:
+            seg = oracle.segments(list(w.numel), w.n_ranks, mode_code(w), w.align, r)
+            ranges += [(int(f), int(f + n)) for _, _, f, _, n in seg]
+    lens = np.array([b - a for a, b in ranges], np.int64)
+    pick = rng.choice(len(ranges), size=n_random, p=lens / lens.sum())
+    offs = (rng.random(n_random) * lens[pick]).astype(np.int64)
+    pts = [np.array([ranges[i][0] for i in pick], np.int64) + offs]
     edges = [0, L - 1]
     starts = np.concatenate([[0], np.cumsum(np.asarray(w.numel, np.int64))])
     edges += list(starts)
