@@ -186,11 +186,11 @@ def recorded_traffic(workload: str):
     return e.get("dram_bytes_per_launch")
 
 
-def step_bytes(phi_padded: int, n_ranks: int, zero3: bool = False) -> int:
+def step_bytes(phi_padded: int, n_ranks: int, n16_out: int = 1) -> int:
     """Algorithmic HBM bytes of one fused step: per element N 16-bit gradient
-    reads, master/m/v read + write (24 B), one 16-bit parameter write."""
-    per = 2 * n_ranks + 24 + 2 + (2 if zero3 else 0)
-    return per * phi_padded
+    reads, master/m/v read + write (24 B), and n16_out 16-bit parameter writes
+    (1: the gathered buffer or, in the ZeRO-3 layout, the rank's shard; 2: both)."""
+    return (2 * n_ranks + 24 + 2 * n16_out) * phi_padded
 
 
 # ----------------------------------------------------------------------------
@@ -254,8 +254,7 @@ def run_reference(args, world, rank):
     from zero_sharded_optimizer_flatten_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
     rate, _ = oracle_rate(w, 1 << 16)
-    total_budget = 60.0
-    n = int(rate * total_budget / max(1, args.steps + args.warmup))
+    n = int(rate * args.ref_budget / max(1, args.steps + args.warmup))
     n = max(4096, min(n, w.phi))
     n -= n % 8
     sample = OracleSample(w, n)
@@ -440,7 +439,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline object")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="parameter group to time (the reported line uses the default)")

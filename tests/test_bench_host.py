@@ -1,0 +1,88 @@
+"""Host logic of bench.py without a GPU: max-over-ranks timing and barriers
+on a 2-rank gloo group, and the reference arm's JSON line."""
+import json
+import multiprocessing as mp
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    w, r, _ = bench.dist_env()
+    dist = bench.init_dist(w, "gloo")
+    bench.barrier(dist)
+    got = bench.max_over_ranks(dist, 1.5 + r)  # rank 1 is the slow one
+    bench.barrier(dist)
+    dist.destroy_process_group()
+    q.put((r, got))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert res == [(0, 2.5), (1, 2.5)]
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3",
+                       "--ref-budget", "1"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in line
+    assert line["impl"] == "reference" and line["unit"] == "params/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3",
+                       "--ref-budget", "1"]) == 0
+    assert capsys.readouterr().out.strip() == ""
+
+
+def test_warmup_floor():
+    sys.path.insert(0, ROOT)
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
+
+
+def test_step_bytes():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.step_bytes(109482240, 8) == 4598254080
+    assert bench.step_bytes(1053760, 4) == 35827840
+    assert bench.step_bytes(212336640, 8, n16_out=2) == 44 * 212336640
