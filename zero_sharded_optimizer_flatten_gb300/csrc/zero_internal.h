@@ -13,9 +13,23 @@ namespace zero {
 
 constexpr int kMaxRanks = 64;     // rank_mask is a uint64_t
 constexpr int kThreads = 256;     // threads per CTA of every kernel
-constexpr int kVec = 8;           // 16-bit elements per 16-byte vector
-constexpr int kTile = kThreads * kVec;  // elements one CTA covers per tile
+constexpr int kVec = 4;           // elements per quad (8 B of 16-bit, 16 B of fp32 data)
+constexpr int kHalf = kThreads * kVec;  // 1024: distance between a thread's two quads
+constexpr int kTile = 2 * kHalf;  // 2048 elements per CTA per tile
 constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
+
+// Resident CTAs per SM the kernels are compiled for (caps registers at 64),
+// and the grid: ZERO_GRID_MULT = 0 launches one CTA per tile; k > 0 caps the
+// grid at k times the resident capacity (the CTAs then stride over tiles).
+// Measured on the BERT-base group (8 replicas): one CTA per tile 6931 GB/s,
+// 32x 6868, 8x 6567, 1x (persistent) 6158 -- the hardware's CTA scheduler
+// spreads the concurrently open DRAM streams better than a grid stride does.
+#ifndef ZERO_MIN_BLOCKS
+#define ZERO_MIN_BLOCKS 4
+#endif
+#ifndef ZERO_GRID_MULT
+#define ZERO_GRID_MULT 0
+#endif
 
 // Binary32 constants of one AdamW step, formed on the host in binary64 and
 // rounded once each (see zero_adamw_hparams).
@@ -32,7 +46,8 @@ enum ScaleMode : int32_t { kScaleNone = 0, kScaleMul = 1, kScaleDiv = 2 };
 // A contiguous run of one rank's elements: flat indices
 // [flat_off, flat_off + len) map to shard indices [shard_off, shard_off + len).
 // vec != 0: flat_off, shard_off and len are multiples of kVec, so the run is
-// processed in 16-byte vectors; otherwise element by element.
+// processed in quads (8-byte 16-bit and 16-byte fp32 accesses); otherwise
+// element by element.
 struct Job {
   int64_t flat_off;
   int64_t shard_off;

@@ -9,12 +9,13 @@
 //
 // Work decomposition: the host cuts each masked rank's owned elements into
 // jobs (runs contiguous in both the flat and the shard index space) and the
-// jobs into tiles of kTile elements.  A persistent grid (SMs x resident CTAs)
-// strides over the tiles; a tile finds its job by binary search in the job
-// table held in the kernel's parameter space.  In a vector job each thread
-// owns 8 consecutive elements (one 16-byte vector of every 16-bit buffer,
-// two of every fp32 buffer); element-wise jobs cover unaligned heads, tails
-// and runs whose flat and shard offsets can never be co-aligned.
+// jobs into tiles of kTile = 2048 elements.  One CTA per tile (the loop
+// strides only past the grid.x limit); a tile finds its job by
+// binary search in the job table held in the kernel's parameter space.  In a
+// vector job each thread owns two quads of 4 consecutive elements, 1024
+// apart, so every warp-wide load and store is one contiguous 256 B (16-bit
+// data) or 512 B (fp32 data) run; element-wise jobs cover unaligned heads,
+// tails and runs whose flat and shard offsets can never be co-aligned.
 //
 // Arithmetic: the reduction adds the replicas in rank order in binary32 and
 // the AdamW update rounds every operation once (__fadd_rn, __fmul_rn,
@@ -77,28 +78,29 @@ struct Fmt<__nv_bfloat16> {
 };
 
 template <class T>
-__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
+__device__ __forceinline__ void unpack4(const uint2& w, float* x) {
   Fmt<T>::unpack(w.x, x[0], x[1]);
   Fmt<T>::unpack(w.y, x[2], x[3]);
-  Fmt<T>::unpack(w.z, x[4], x[5]);
-  Fmt<T>::unpack(w.w, x[6], x[7]);
 }
 
 template <class T>
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-  return make_uint4(Fmt<T>::pack(x[0], x[1]), Fmt<T>::pack(x[2], x[3]),
-                    Fmt<T>::pack(x[4], x[5]), Fmt<T>::pack(x[6], x[7]));
+__device__ __forceinline__ uint2 pack4(const float* x) {
+  return make_uint2(Fmt<T>::pack(x[0], x[1]), Fmt<T>::pack(x[2], x[3]));
 }
 
 // ---------------------------------------------------------------------------
 // memory access
+//
+// A thread owns two quads (4 consecutive elements each) of a 2048-element
+// tile: job offsets e0 = base + 4*tid and e1 = e0 + 1024.  Every warp-wide
+// access is then contiguous (256 B of 16-bit data, 512 B of fp32 data per
+// instruction), which keeps the DRAM request stream dense.
 
-// Gradient replicas are read exactly once: non-coherent path, no L1 allocation.
-__device__ __forceinline__ uint4 ld_once(const void* p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+// Gradient replicas and shard copies are read exactly once: non-coherent
+// path, no L1 allocation.
+__device__ __forceinline__ uint2 ld_once8(const void* p) {
+  uint2 r;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
 
@@ -116,9 +118,18 @@ __device__ __forceinline__ void st_state(float* p, const float4& v) {
   __stcs(reinterpret_cast<float4*>(p), v);
 }
 
-__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
-  __stcs(reinterpret_cast<uint4*>(p), v);
+__device__ __forceinline__ void st_quad16(void* p, const uint2& v) {
+  __stcs(reinterpret_cast<uint2*>(p), v);
 }
+
+__device__ __forceinline__ void split(const float4& v, float* x) {
+  x[0] = v.x;
+  x[1] = v.y;
+  x[2] = v.z;
+  x[3] = v.w;
+}
+
+__device__ __forceinline__ float4 join(const float* x) { return make_float4(x[0], x[1], x[2], x[3]); }
 
 // ---------------------------------------------------------------------------
 // arithmetic
@@ -139,29 +150,41 @@ __device__ __forceinline__ void adamw1(const StepScalars& s, float g, float& p, 
   p = __fsub_rn(p, __fmul_rn(s.ss, __fdiv_rn(m, den)));
 }
 
-// Rank-ordered binary32 sum of the N replicas' 8 elements at flat index f.
-// NR > 0: N known at compile time, all N vectors are requested before the
-// first add (N outstanding 16-byte loads per thread).  NR == 0: any N.
+// Rank-ordered binary32 sum of the N replicas at the thread's two quads
+// (flat indices f0.., f1..); g[0..3] for quad 0, g[4..7] for quad 1 (zero
+// when `two` is false).  NR > 0: N fixed at compile time and every replica's
+// two 8-byte loads are issued before the first add.  NR == 0: any N.
 template <class T, int NR>
-__device__ __forceinline__ void reduce8(const LaunchArgs& a, int64_t f, float (&g)[8]) {
+__device__ __forceinline__ void reduce_quads(const LaunchArgs& a, int64_t f0, int64_t f1,
+                                             bool two, float (&g)[8]) {
+  const uint2 z = make_uint2(0u, 0u);
   if constexpr (NR > 0) {
-    uint4 w[NR];
+    uint2 w0[NR], w1[NR];
 #pragma unroll
-    for (int q = 0; q < NR; ++q)
-      w[q] = ld_once(static_cast<const uint16_t*>(a.grads[q]) + f);
-    unpack8<T>(w[0], g);
+    for (int q = 0; q < NR; ++q) {
+      const uint16_t* base = static_cast<const uint16_t*>(a.grads[q]);
+      w0[q] = ld_once8(base + f0);
+      w1[q] = two ? ld_once8(base + f1) : z;
+    }
+    unpack4<T>(w0[0], g);
+    unpack4<T>(w1[0], g + 4);
 #pragma unroll
     for (int q = 1; q < NR; ++q) {
       float h[8];
-      unpack8<T>(w[q], h);
+      unpack4<T>(w0[q], h);
+      unpack4<T>(w1[q], h + 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k) g[k] = __fadd_rn(g[k], h[k]);
     }
   } else {
-    unpack8<T>(ld_once(static_cast<const uint16_t*>(a.grads[0]) + f), g);
+    const uint16_t* b0 = static_cast<const uint16_t*>(a.grads[0]);
+    unpack4<T>(ld_once8(b0 + f0), g);
+    unpack4<T>(two ? ld_once8(b0 + f1) : z, g + 4);
     for (int q = 1; q < a.n_ranks; ++q) {
+      const uint16_t* base = static_cast<const uint16_t*>(a.grads[q]);
       float h[8];
-      unpack8<T>(ld_once(static_cast<const uint16_t*>(a.grads[q]) + f), h);
+      unpack4<T>(ld_once8(base + f0), h);
+      unpack4<T>(two ? ld_once8(base + f1) : z, h + 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k) g[k] = __fadd_rn(g[k], h[k]);
     }
@@ -180,6 +203,27 @@ __device__ __forceinline__ float reduce1(const LaunchArgs& a, int64_t f) {
   return scale_grad(a, g);
 }
 
+// fp32 state of the thread's two quads: x[0..3] at i0, x[4..7] at i1.
+__device__ __forceinline__ void load_state2(const float* base, int64_t i0, int64_t i1, bool two,
+                                            float (&x)[8]) {
+  split(ld_state(base + i0), x);
+  split(two ? ld_state(base + i1) : make_float4(0.f, 0.f, 0.f, 0.f), x + 4);
+}
+
+__device__ __forceinline__ void store_state2(float* base, int64_t i0, int64_t i1, bool two,
+                                             const float (&x)[8]) {
+  st_state(base + i0, join(x));
+  if (two) st_state(base + i1, join(x + 4));
+}
+
+template <class T>
+__device__ __forceinline__ void store_16x2(void* base, int64_t i0, int64_t i1, bool two,
+                                           const float (&x)[8]) {
+  uint16_t* b = static_cast<uint16_t*>(base);
+  st_quad16(b + i0, pack4<T>(x));
+  if (two) st_quad16(b + i1, pack4<T>(x + 4));
+}
+
 // ---------------------------------------------------------------------------
 // tile -> job
 
@@ -195,8 +239,9 @@ __device__ __forceinline__ int find_job(const LaunchArgs& a, int64_t tile) {
   return lo;
 }
 
-// Calls body_vec(job, e) for the 8-element vector at job offset e, or
-// body_one(job, e) for single elements, over every tile of the launch.
+// Calls body_vec(job, e0, two) for the thread's quads at job offsets e0 and
+// e0 + kHalf (the second only when `two`), or body_one(job, e) for single
+// elements, over every tile of the launch.
 template <class BodyVec, class BodyOne>
 __device__ __forceinline__ void for_each_tile(const LaunchArgs& a, BodyVec body_vec,
                                               BodyOne body_one) {
@@ -204,11 +249,11 @@ __device__ __forceinline__ void for_each_tile(const LaunchArgs& a, BodyVec body_
     const Job& jb = a.jobs[find_job(a, tile)];
     const int64_t base = (tile - jb.tile_begin) * kTile;
     if (jb.vec) {
-      const int64_t e = base + static_cast<int64_t>(threadIdx.x) * kVec;
-      if (e < jb.len) body_vec(jb, e);
+      const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
+      if (e0 < jb.len) body_vec(jb, e0, e0 + kHalf < jb.len);
     } else {
 #pragma unroll 1
-      for (int k = 0; k < kVec; ++k) {
+      for (int k = 0; k < kTile / kThreads; ++k) {
         const int64_t e = base + k * kThreads + threadIdx.x;
         if (e < jb.len) body_one(jb, e);
       }
@@ -221,34 +266,25 @@ __device__ __forceinline__ void for_each_tile(const LaunchArgs& a, BodyVec body_
 
 // Fused step: reduce-scatter + AdamW + cast + all-gather.
 template <class T, int NR>
-__global__ void __launch_bounds__(kThreads) k_step(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_step(const __grid_constant__ LaunchArgs a) {
   for_each_tile(
       a,
-      [&](const Job& jb, int64_t e) {
-        const int64_t f = jb.flat_off + e, i = jb.shard_off + e;
+      [&](const Job& jb, int64_t e0, bool two) {
         const int r = jb.rank;
-        float* pm = a.master[r] + i;
-        float* mm = a.m[r] + i;
-        float* vm = a.v[r] + i;
-        float g[8];
-        reduce8<T, NR>(a, f, g);
-        const float4 p0 = ld_state(pm), p1 = ld_state(pm + 4);
-        const float4 m0 = ld_state(mm), m1 = ld_state(mm + 4);
-        const float4 v0 = ld_state(vm), v1 = ld_state(vm + 4);
-        float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
+        const int64_t f1 = f0 + kHalf, i1 = i0 + kHalf;
+        float g[8], p[8], m[8], v[8];
+        reduce_quads<T, NR>(a, f0, f1, two, g);
+        load_state2(a.master[r], i0, i1, two, p);
+        load_state2(a.m[r], i0, i1, two, m);
+        load_state2(a.v[r], i0, i1, two, v);
 #pragma unroll
         for (int k = 0; k < 8; ++k) adamw1(a.sc, g[k], p[k], m[k], v[k]);
-        st_state(pm, make_float4(p[0], p[1], p[2], p[3]));
-        st_state(pm + 4, make_float4(p[4], p[5], p[6], p[7]));
-        st_state(mm, make_float4(m[0], m[1], m[2], m[3]));
-        st_state(mm + 4, make_float4(m[4], m[5], m[6], m[7]));
-        st_state(vm, make_float4(v[0], v[1], v[2], v[3]));
-        st_state(vm + 4, make_float4(v[4], v[5], v[6], v[7]));
-        const uint4 o = pack8<T>(p);
-        if (a.full16) st_vec(static_cast<uint16_t*>(a.full16) + f, o);
-        if (a.shard16[r]) st_vec(static_cast<uint16_t*>(a.shard16[r]) + i, o);
+        store_state2(a.master[r], i0, i1, two, p);
+        store_state2(a.m[r], i0, i1, two, m);
+        store_state2(a.v[r], i0, i1, two, v);
+        if (a.full16) store_16x2<T>(a.full16, f0, f1, two, p);
+        if (a.shard16[r]) store_16x2<T>(a.shard16[r], i0, i1, two, p);
       },
       [&](const Job& jb, int64_t e) {
         const int64_t f = jb.flat_off + e, i = jb.shard_off + e;
@@ -267,15 +303,14 @@ __global__ void __launch_bounds__(kThreads) k_step(const __grid_constant__ Launc
 
 // Reduce-scatter alone: fp32 gradient shards.
 template <class T, int NR>
-__global__ void __launch_bounds__(kThreads) k_reduce_scatter(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_reduce_scatter(const __grid_constant__ LaunchArgs a) {
   for_each_tile(
       a,
-      [&](const Job& jb, int64_t e) {
+      [&](const Job& jb, int64_t e0, bool two) {
         float g[8];
-        reduce8<T, NR>(a, jb.flat_off + e, g);
-        float* out = a.gshard[jb.rank] + jb.shard_off + e;
-        st_state(out, make_float4(g[0], g[1], g[2], g[3]));
-        st_state(out + 4, make_float4(g[4], g[5], g[6], g[7]));
+        const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
+        reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
+        store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
       },
       [&](const Job& jb, int64_t e) {
         a.gshard[jb.rank][jb.shard_off + e] = reduce1<T, NR>(a, jb.flat_off + e);
@@ -284,33 +319,23 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(const __grid_consta
 
 // AdamW + cast on fp32 gradient shards.
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw(const __grid_constant__ LaunchArgs a) {
   for_each_tile(
       a,
-      [&](const Job& jb, int64_t e) {
-        const int64_t i = jb.shard_off + e;
+      [&](const Job& jb, int64_t e0, bool two) {
         const int r = jb.rank;
-        float* pm = a.master[r] + i;
-        float* mm = a.m[r] + i;
-        float* vm = a.v[r] + i;
-        const float* gm = a.gshard[r] + i;
-        const float4 g0 = ld_state(gm), g1 = ld_state(gm + 4);
-        const float4 p0 = ld_state(pm), p1 = ld_state(pm + 4);
-        const float4 m0 = ld_state(mm), m1 = ld_state(mm + 4);
-        const float4 v0 = ld_state(vm), v1 = ld_state(vm + 4);
-        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const int64_t i0 = jb.shard_off + e0, i1 = i0 + kHalf;
+        float g[8], p[8], m[8], v[8];
+        load_state2(a.gshard[r], i0, i1, two, g);
+        load_state2(a.master[r], i0, i1, two, p);
+        load_state2(a.m[r], i0, i1, two, m);
+        load_state2(a.v[r], i0, i1, two, v);
 #pragma unroll
         for (int k = 0; k < 8; ++k) adamw1(a.sc, g[k], p[k], m[k], v[k]);
-        st_state(pm, make_float4(p[0], p[1], p[2], p[3]));
-        st_state(pm + 4, make_float4(p[4], p[5], p[6], p[7]));
-        st_state(mm, make_float4(m[0], m[1], m[2], m[3]));
-        st_state(mm + 4, make_float4(m[4], m[5], m[6], m[7]));
-        st_state(vm, make_float4(v[0], v[1], v[2], v[3]));
-        st_state(vm + 4, make_float4(v[4], v[5], v[6], v[7]));
-        if (a.shard16[r]) st_vec(static_cast<uint16_t*>(a.shard16[r]) + i, pack8<T>(p));
+        store_state2(a.master[r], i0, i1, two, p);
+        store_state2(a.m[r], i0, i1, two, m);
+        store_state2(a.v[r], i0, i1, two, v);
+        if (a.shard16[r]) store_16x2<T>(a.shard16[r], i0, i1, two, p);
       },
       [&](const Job& jb, int64_t e) {
         const int64_t i = jb.shard_off + e;
@@ -326,12 +351,16 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Laun
 
 // All-gather: copy each rank's 16-bit shard into the flat buffer.
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_allgather(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_allgather(const __grid_constant__ LaunchArgs a) {
   for_each_tile(
       a,
-      [&](const Job& jb, int64_t e) {
-        const uint4 w = ld_once(static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e);
-        st_vec(static_cast<uint16_t*>(a.full16) + jb.flat_off + e, w);
+      [&](const Job& jb, int64_t e0, bool two) {
+        const uint16_t* src = static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e0;
+        uint16_t* dst = static_cast<uint16_t*>(a.full16) + jb.flat_off + e0;
+        const uint2 w0 = ld_once8(src);
+        const uint2 w1 = two ? ld_once8(src + kHalf) : make_uint2(0u, 0u);
+        st_quad16(dst, w0);
+        if (two) st_quad16(dst + kHalf, w1);
       },
       [&](const Job& jb, int64_t e) {
         static_cast<uint16_t*>(a.full16)[jb.flat_off + e] =
@@ -341,21 +370,20 @@ __global__ void __launch_bounds__(kThreads) k_allgather(const __grid_constant__ 
 
 // Initialise a rank's fp32 master from its 16-bit partition; zero m and v.
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_init(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_init(const __grid_constant__ LaunchArgs a) {
   for_each_tile(
       a,
-      [&](const Job& jb, int64_t e) {
-        const int64_t i = jb.shard_off + e;
+      [&](const Job& jb, int64_t e0, bool two) {
         const int r = jb.rank;
+        const int64_t i0 = jb.shard_off + e0, i1 = i0 + kHalf;
+        const uint16_t* src = static_cast<const uint16_t*>(a.full16) + jb.flat_off + e0;
         float p[8];
-        unpack8<T>(ld_once(static_cast<const uint16_t*>(a.full16) + jb.flat_off + e), p);
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        st_state(a.master[r] + i, make_float4(p[0], p[1], p[2], p[3]));
-        st_state(a.master[r] + i + 4, make_float4(p[4], p[5], p[6], p[7]));
-        st_state(a.m[r] + i, z);
-        st_state(a.m[r] + i + 4, z);
-        st_state(a.v[r] + i, z);
-        st_state(a.v[r] + i + 4, z);
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        unpack4<T>(ld_once8(src), p);
+        unpack4<T>(two ? ld_once8(src + kHalf) : make_uint2(0u, 0u), p + 4);
+        store_state2(a.master[r], i0, i1, two, p);
+        store_state2(a.m[r], i0, i1, two, z);
+        store_state2(a.v[r], i0, i1, two, z);
       },
       [&](const Job& jb, int64_t e) {
         const int64_t i = jb.shard_off + e;
@@ -370,9 +398,8 @@ __global__ void __launch_bounds__(kThreads) k_init(const __grid_constant__ Launc
 // ---------------------------------------------------------------------------
 // launch (host)
 
-// Grid of a persistent launch of kernel `fn`: resident CTAs per SM times the
-// SM count of the current device, capped by the tile count.
-int persistent_grid(const void* fn, int64_t n_tiles);
+// Grid of a launch of kernel `fn` over n_tiles tiles (see ZERO_GRID_MULT).
+int grid_for(const void* fn, int64_t n_tiles);
 
 template <class T, template <class, int> class Pick>
 const void* by_ranks(int n) {
@@ -409,7 +436,7 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kAllgather: fn = reinterpret_cast<const void*>(&k_allgather<T>); break;
     case Kind::kInit: fn = reinterpret_cast<const void*>(&k_init<T>); break;
   }
-  const int grid = persistent_grid(fn, a.n_tiles);
+  const int grid = grid_for(fn, a.n_tiles);
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
   return static_cast<int>(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s));

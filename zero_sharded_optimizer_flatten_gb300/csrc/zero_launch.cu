@@ -1,4 +1,4 @@
-// Kernel dispatch and persistent-grid sizing.
+// Kernel dispatch and grid sizing.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -12,7 +12,9 @@ namespace zero {
 extern template int launch_typed<__half>(Kind, const LaunchArgs&, cudaStream_t);
 extern template int launch_typed<__nv_bfloat16>(Kind, const LaunchArgs&, cudaStream_t);
 
-int persistent_grid(const void* fn, int64_t n_tiles) {
+int grid_for(const void* fn, int64_t n_tiles) {
+  constexpr int64_t kMaxGrid = 0x7fffffff;  // grid.x limit; CTAs stride beyond it
+  if (ZERO_GRID_MULT == 0) return static_cast<int>(n_tiles < kMaxGrid ? n_tiles : kMaxGrid);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   static std::mutex mu;
@@ -29,7 +31,7 @@ int persistent_grid(const void* fn, int64_t n_tiles) {
         return -1;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -1;
-      slots = (per_sm > 0 ? per_sm : 1) * sms;
+      slots = (per_sm > 0 ? per_sm : 1) * sms * ZERO_GRID_MULT;
       cache[{fn, dev}] = slots;
     }
   }
