@@ -283,6 +283,128 @@ def run_reference(args, world, rank):
     return 0
 
 
+class FlatRunner:
+    """One fused step over the masked ranks of a flat or round-robin group
+    (bucketed if the workload says so).  Gradient buffers hold only the flat
+    range the masked ranks own."""
+
+    def __init__(self, w, dev, grad_sets):
+        import torch
+
+        import zero_sharded_optimizer_flatten_gb300 as Z
+        from zero_sharded_optimizer_flatten_gb300 import workloads as W
+        self.Z, self.w, self.dev = Z, w, dev
+        self.plan = plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+        self.mask = w.mask
+        self.ext = ext = plan.flat_extent(self.mask)
+        self.hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
+        p16 = W.fill(w, "param", 0, 0, 0, ext, torch.empty(ext, dtype=w.torch_dtype, device=dev))
+        self.full16 = torch.zeros_like(p16)
+        S = [plan.shard_len(r) if (self.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+        self.master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+        self.m = [torch.empty_like(x) for x in self.master]
+        self.v = [torch.empty_like(x) for x in self.master]
+        Z.zero_init_shards(plan, p16, self.master, self.m, self.v, rank_mask=self.mask)
+        del p16
+        self.grads = [[W.grads16(w, s + 1, q, dev, 0, ext) for q in range(w.n_ranks)]
+                      for s in range(grad_sets)]
+        self.calls = [Z.ZeroStep(plan, g, w.op, self.master, self.m, self.v, self.full16, None,
+                                 self.hp, rank_mask=self.mask, bucket_elems=w.bucket_elems)
+                      for g in self.grads]
+        self.elems = sum(S)                       # work units per step
+        self.padded = plan.padded
+        self.bytes_per_step = step_bytes(self.elems, w.n_ranks)
+        self.kernel = KERNEL_PREFIX
+
+    def step(self, t, events=None):
+        if events is not None:
+            events[0].record()
+        self.calls[t % len(self.calls)](t)
+        if events is not None:
+            events[1].record()
+
+    def e2e(self, t0, steps):
+        """The public API with host buffers: pinned gradients in, updated
+        16-bit parameters out, every step.  Returns (seconds, h2d, d2h)."""
+        import torch
+        w, Z = self.w, self.Z
+        host_g = [torch.empty(self.ext, dtype=w.torch_dtype, pin_memory=True)
+                  for _ in range(w.n_ranks)]
+        for q in range(w.n_ranks):
+            host_g[q].copy_(self.grads[0][q])
+        host_out = torch.empty(self.ext, dtype=w.torch_dtype, pin_memory=True)
+        dev_g = self.grads[0]
+
+        def one(t):
+            for q in range(w.n_ranks):
+                dev_g[q].copy_(host_g[q], non_blocking=True)
+            Z.zero_step(self.plan, dev_g, w.op, self.master, self.m, self.v, self.full16, None,
+                        self.hp, t, rank_mask=self.mask, bucket_elems=w.bucket_elems)
+            host_out.copy_(self.full16, non_blocking=True)
+
+        t = t0
+        for _ in range(2):
+            t += 1
+            one(t)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            t += 1
+            one(t)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3, w.n_ranks * self.ext * 2, self.ext * 2
+
+
+class Zero3Runner:
+    """The ZeRO-3 layer stream: per layer, all-gather the 8 ranks' 16-bit
+    shards into the layer buffer, then the fused step writing each rank's
+    shard (the next gather's source).  One gradient set is shared by all
+    layers (the backward pass refills one buffer per layer)."""
+
+    def __init__(self, w, dev, layer_states):
+        import torch
+
+        import zero_sharded_optimizer_flatten_gb300 as Z
+        from zero_sharded_optimizer_flatten_gb300 import workloads as W
+        self.Z, self.w, self.dev = Z, w, dev
+        self.plan = plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+        self.hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
+        L = plan.padded
+        S = [plan.shard_len(r) for r in range(w.n_ranks)]
+        self.layer_buf = torch.empty(L, dtype=w.torch_dtype, device=dev)
+        self.grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+        self.n_states = min(w.layers, layer_states)
+        self.shards, self.calls = [], []
+        for layer in range(self.n_states):
+            p16 = W.params16(w, dev, layer=layer)
+            sh = [p16[sum(S[:r]):sum(S[:r]) + S[r]].clone() for r in range(w.n_ranks)]
+            master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+            m = [torch.empty_like(x) for x in master]
+            v = [torch.empty_like(x) for x in master]
+            Z.zero_init_shards(plan, p16, master, m, v)
+            del p16
+            self.shards.append(sh)
+            self.calls.append(Z.ZeroStep(plan, self.grads, w.op, master, m, v, None, sh, self.hp))
+        self.layers = w.layers
+        self.elems = w.layers * plan.padded
+        self.bytes_per_step = w.layers * (step_bytes(plan.padded, w.n_ranks) + 4 * plan.padded)
+        self.kernel_bytes = step_bytes(plan.padded, w.n_ranks)  # per k_step launch
+        self.kernel = KERNEL_PREFIX
+
+    def step(self, t, events=None):
+        for layer in range(self.layers):
+            k = layer % self.n_states
+            self.Z.zero_allgather(self.plan, self.shards[k], self.layer_buf)
+            if events is not None:
+                events[layer][0].record()
+            self.calls[k](t)
+            if events is not None:
+                events[layer][1].record()
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -295,34 +417,29 @@ def run_gpu(args, world, rank, local):
     dist = init_dist(world, "nccl")
     w = W.WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
-    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
-    P = plan.padded
-    hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
-
-    p16 = W.params16(w, dev)
-    full16 = torch.zeros_like(p16)
-    S = [plan.shard_len(r) for r in range(w.n_ranks)]
-    master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
-    m = [torch.empty_like(x) for x in master]
-    v = [torch.empty_like(x) for x in master]
-    Z.zero_init_shards(plan, p16, master, m, v)
-    n_sets = args.grad_sets  # distinct gradient sets, alternated step to step
-    grads = [[W.grads16(w, s + 1, q, dev) for q in range(w.n_ranks)] for s in range(n_sets)]
-    steps = [Z.ZeroStep(plan, g, w.op, master, m, v, full16, None, hp) for g in grads]
+    if w.zero3:
+        run = Zero3Runner(w, dev, args.layer_states)
+    else:
+        run = FlatRunner(w, dev, args.grad_sets)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
     t = 0
     for _ in range(args.warmup):
         t += 1
-        steps[t % n_sets](t)
+        run.step(t)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+
+    def pair():
+        return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    if w.zero3:
+        ev = [[pair() for _ in range(run.layers)] for _ in range(args.steps)]
+    else:
+        ev = [pair() for _ in range(args.steps)]
     barrier(dist, local)
     torch.cuda.synchronize(dev)
     launches0 = Z.zero_launch_count()
@@ -332,9 +449,7 @@ def run_gpu(args, world, rank, local):
     start.record(stream)
     for k in range(args.steps):
         t += 1
-        ev[k][0].record(stream)
-        steps[t % n_sets](t)
-        ev[k][1].record(stream)
+        run.step(t, ev[k])
     stop.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -343,44 +458,27 @@ def run_gpu(args, world, rank, local):
     clocks.stop()
     elapsed = start.elapsed_time(stop) / 1e3
     elapsed = max_over_ranks(dist, elapsed, local)
-    kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
+    if w.zero3:
+        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
+        bytes_per_launch = run.kernel_bytes
+    else:
+        kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
+        bytes_per_launch = run.bytes_per_step
 
-    # end to end through the public API: pinned host gradients in, updated
-    # parameters out, every step
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    host_g = [torch.empty(P, dtype=w.torch_dtype, pin_memory=True) for _ in range(w.n_ranks)]
-    for q in range(w.n_ranks):
-        host_g[q].copy_(grads[0][q])
-    host_out = torch.empty(P, dtype=w.torch_dtype, pin_memory=True)
-    dev_g = grads[0]
-    for _ in range(2):
-        t += 1
-        for q in range(w.n_ranks):
-            dev_g[q].copy_(host_g[q], non_blocking=True)
-        Z.zero_step(plan, dev_g, w.op, master, m, v, full16, None, hp, t)
-        host_out.copy_(full16, non_blocking=True)
-    torch.cuda.synchronize(dev)
-    barrier(dist, local)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        t += 1
-        for q in range(w.n_ranks):
-            dev_g[q].copy_(host_g[q], non_blocking=True)
-        Z.zero_step(plan, dev_g, w.op, master, m, v, full16, None, hp, t)
-        host_out.copy_(full16, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_s = max_over_ranks(dist, e0.elapsed_time(e1) / 1e3, local)
+    e2e = None
+    if not w.zero3:
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        e2e_s, h2d, d2h = run.e2e(t, e2e_steps)
+        e2e_s = max_over_ranks(dist, e2e_s, local)
+        e2e = {"value": run.elems * e2e_steps * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
-    bytes_per_launch = step_bytes(P, w.n_ranks)
     peak, peak_src = measured_peaks()
     achieved = bytes_per_launch / kernel_s / 1e9
     line = {
         "impl": "gb300",
         "metric": METRIC,
-        "value": w.phi * args.steps * world / elapsed,
+        "value": run.elems * args.steps * world / elapsed,
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -394,12 +492,12 @@ def run_gpu(args, world, rank, local):
         "config": {
             "workload": w.title,
             "phi": w.phi,
-            "padded": P,
+            "elements_per_step": run.elems,
             "virtual_ranks": w.n_ranks,
-            "storage": "bf16 params and gradients, fp32 master/m/v",
+            "storage": f"{w.dtype} params and gradients, fp32 master/m/v",
             "parallelism": f"{world} independent replica(s); {w.n_ranks} virtual ranks each",
-            "l2": f"inputs larger than L2: {bytes_per_launch / 1e9:.2f} GB touched per step",
-            "hbm_gbs_per_step": bytes_per_launch / (elapsed / args.steps) / 1e9,
+            "l2": f"inputs larger than L2: {run.bytes_per_step / 1e9:.2f} GB touched per step",
+            "hbm_gbs_per_step": run.bytes_per_step / (elapsed / args.steps) / 1e9,
         },
         "roofline": {
             "bound": "hbm",
@@ -408,21 +506,18 @@ def run_gpu(args, world, rank, local):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": recorded_traffic(args.workload),
-            "kernel": KERNEL_PREFIX,
+            "kernel": run.kernel,
             "bytes_per_launch": bytes_per_launch,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                            else "fallback 6.8 TB/s",
         },
-        "e2e": {
-            "value": w.phi * e2e_steps * world / e2e_s,
-            "unit": UNIT,
-            "h2d_bytes_per_step": w.n_ranks * P * 2,
-            "d2h_bytes_per_step": P * 2,
-            "steps": e2e_steps,
-        },
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(wall0, wall1),
     }
+    if w.zero3:
+        line["config"]["layer_states"] = run.n_states
+        line["config"]["layers"] = run.layers
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     if rank == 0:
@@ -448,6 +543,8 @@ def main(argv=None):
                     help="parameter group to time (the reported line uses the default)")
     ap.add_argument("--grad-sets", type=int, default=2,
                     help="distinct gradient sets resident in HBM, alternated per step")
+    ap.add_argument("--layer-states", type=int, default=40,
+                    help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
