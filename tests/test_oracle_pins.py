@@ -67,6 +67,8 @@ def test_rounding_special_cases():
     assert r16(65504.0) == 0x7BFF                   # largest finite
     assert r16(65519.99) == 0x7BFF                  # below the midpoint to 2^16
     assert r16(65520.0) == 0x7C00                   # midpoint: ties to even -> overflow
+    assert r16(70000.0) == 0x7C00                   # beyond the largest binade -> +inf
+    assert r16(-1e30) == 0xFC00
     assert r16(2.0 ** -24) == 0x0001                # smallest subnormal
     assert r16(2.0 ** -25) == 0x0000                # tie between 0 and 2^-24 -> even (0)
     assert r16(1.5 * 2.0 ** -25) == 0x0001
