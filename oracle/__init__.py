@@ -26,6 +26,11 @@ tests in tests/test_oracle_pins.py):
                          pure decay for zero gradients
   step                   partition invariance (sharded == unsharded, bit for
                          bit) across N, A and both partition modes
+  step_amp               S = 1 without clipping == step (bit-exact); a power-of-
+                         two loss scale on exactly scaled gradients == step on
+                         the unscaled ones (bit-exact); clipping == torch's
+                         clip_grad_norm_ followed by torch.optim.AdamW; the
+                         loss-scale trajectory of the configuration keys
 """
 from __future__ import annotations
 
@@ -303,3 +308,59 @@ def allgather(numel, n_ranks: int, mode: int, align: int, shard16, full16,
     _check(lib().orc_allgather(p, len(arr), n_ranks, mode, align,
                                ctypes.cast(_ptr_array(shard16), vpp), _ptr(full16), rank_mask),
            "allgather")
+
+
+# ----------------------------------------------------------------------------
+# mixed-precision controls (loss scaling, overflow skip, clipping)
+
+
+class AmpConfig(ctypes.Structure):
+    _fields_ = [("init_scale", ctypes.c_double), ("min_scale", ctypes.c_double),
+                ("window", ctypes.c_int32), ("hysteresis", ctypes.c_int32),
+                ("max_norm", ctypes.c_double)]
+
+
+class AmpState(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_double), ("norm", ctypes.c_double),
+                ("step", ctypes.c_int64), ("skipped", ctypes.c_int64),
+                ("good_steps", ctypes.c_int32), ("hysteresis_left", ctypes.c_int32),
+                ("overflow", ctypes.c_int32), ("coef", ctypes.c_float)]
+
+
+def amp_config(init_scale=65536.0, min_scale=1.0, window=1000, hysteresis=2, max_norm=0.0):
+    return AmpConfig(init_scale, min_scale, window, hysteresis, max_norm)
+
+
+def amp_init(cfg: AmpConfig) -> AmpState:
+    L = lib()
+    L.orc_amp_init.argtypes = [ctypes.POINTER(AmpConfig), ctypes.POINTER(AmpState)]
+    L.orc_amp_init.restype = None
+    st = AmpState()
+    L.orc_amp_init(ctypes.byref(cfg), ctypes.byref(st))
+    return st
+
+
+def step_amp(numel, n_ranks: int, mode: int, align: int, dtype: int, op: int, grads, master, m,
+             v, full16, shard16, hp: Hparams, cfg: AmpConfig, state: AmpState,
+             rank_mask: int | None = None):
+    """One mixed-precision step (in place on master/m/v/full16 and state)."""
+    L = lib()
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    L.orc_step_amp.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vpp, vpp, vpp,
+                               vpp, ctypes.c_void_p, vpp, ctypes.POINTER(Hparams),
+                               ctypes.POINTER(AmpConfig), ctypes.POINTER(AmpState),
+                               ctypes.c_uint64]
+    L.orc_step_amp.restype = ctypes.c_int
+    arr, p = _i64(numel)
+    if rank_mask is None:
+        rank_mask = (1 << n_ranks) - 1
+    sh = _ptr_array(shard16) if shard16 is not None else None
+    _check(L.orc_step_amp(p, len(arr), n_ranks, mode, align, dtype, op,
+                          ctypes.cast(_ptr_array(grads), vpp),
+                          ctypes.cast(_ptr_array(master), vpp), ctypes.cast(_ptr_array(m), vpp),
+                          ctypes.cast(_ptr_array(v), vpp),
+                          0 if full16 is None else _ptr(full16),
+                          None if sh is None else ctypes.cast(sh, vpp), ctypes.byref(hp),
+                          ctypes.byref(cfg), ctypes.byref(state), rank_mask), "step_amp")

@@ -483,3 +483,143 @@ int orc_allgather(const int64_t* numel, int32_t n_tensors, int32_t N, int32_t mo
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Mixed-precision controls: dynamic loss scaling with overflow skip,  */
+/* global-norm gradient clipping                                       */
+/* ------------------------------------------------------------------ */
+/*
+ * The pages give these only as configuration ("ZeRO ... 实操" (wmrh.cn)
+ * §3.1 and §3.3 ds_config: fp16 loss_scale 0 = dynamic, loss_scale_window
+ * 1000, hysteresis 2, min_loss_scale 1; gradient_clipping).  Reading taken:
+ *  - the gradients carry the loss scale S; the reduced gradient g (sum or
+ *    average of the replicas, as in the plain step) is checked for
+ *    non-finite values through its squared norm  sumsq = sum g^2  (binary64,
+ *    exact squares);
+ *  - non-finite sumsq: the update is skipped (no state, parameter or step
+ *    count changes); if more than one overflow is still tolerated the
+ *    tolerance drops by one, else S halves (not below min_scale); the
+ *    run of good steps restarts;
+ *  - finite: norm = sqrt(sumsq)/S is the unscaled global norm; with
+ *    max_norm > 0 the clip factor is min(1, max_norm / (norm + 1e-6))
+ *    (as torch.nn.utils.clip_grad_norm_), else 1; the gradient multiplier
+ *    coef = clip / S is rounded once to binary32 and every element uses
+ *    g * coef (one rounding) in the AdamW update of step t = steps + 1;
+ *    after `window` consecutive good steps S doubles and the overflow
+ *    tolerance is restored.
+ */
+typedef struct {
+  double init_scale, min_scale;
+  int32_t window, hysteresis;
+  double max_norm;
+} orc_amp_config;
+
+typedef struct {
+  double scale, norm;
+  int64_t step, skipped;
+  int32_t good_steps, hysteresis_left, overflow;
+  float coef;
+} orc_amp_state;
+
+void orc_amp_init(const orc_amp_config* c, orc_amp_state* s) {
+  s->scale = c->init_scale;
+  s->norm = 0.0;
+  s->step = 0;
+  s->skipped = 0;
+  s->good_steps = 0;
+  s->hysteresis_left = c->hysteresis;
+  s->overflow = 0;
+  s->coef = 1.0f;
+}
+
+int orc_step_amp(const int64_t* numel, int32_t n_tensors, int32_t N, int32_t mode, int32_t A,
+                 int32_t dtype, int32_t op, const uint16_t* const* grads, float* const* master,
+                 float* const* m, float* const* v, uint16_t* full16, uint16_t* const* shard16,
+                 const orc_hparams* h, const orc_amp_config* c, orc_amp_state* st,
+                 uint64_t rank_mask) {
+  float* gbuf[64] = {0};
+  int64_t* segs[64] = {0};
+  int64_t nsegs[64] = {0};
+  double sumsq = 0.0;
+  int rc = 0;
+  if (N > 64) return 1;
+  /* 1. reduce every owned element and accumulate the squared norm */
+  for (int32_t r = 0; r < N && !rc; r++) {
+    if (!((rank_mask >> r) & 1)) continue;
+    if (for_each_segment(numel, n_tensors, N, mode, A, r, &segs[r], &nsegs[r])) {
+      rc = 1;
+      break;
+    }
+    int64_t total = 0;
+    for (int64_t j = 0; j < nsegs[r]; j++) total += segs[r][4 * nsegs[r] + j];
+    gbuf[r] = (float*)malloc(sizeof(float) * (size_t)(total ? total : 1));
+    if (!gbuf[r]) {
+      rc = 1;
+      break;
+    }
+    for (int64_t j = 0; j < nsegs[r]; j++)
+      for (int64_t e = 0; e < segs[r][4 * nsegs[r] + j]; e++) {
+        int64_t f = segs[r][2 * nsegs[r] + j] + e, i = segs[r][3 * nsegs[r] + j] + e;
+        float acc = to_f32(dtype, grads[0][f]);
+        for (int32_t q = 1; q < N; q++) acc = acc + to_f32(dtype, grads[q][f]);
+        if (op == ORC_AVG) acc = acc / (float)N;
+        gbuf[r][i] = acc;
+        sumsq += (double)acc * (double)acc;
+      }
+  }
+  if (!rc) {
+    /* 2. the loss-scale decision */
+    double S = st->scale;
+    if (!isfinite(sumsq)) {
+      st->overflow = 1;
+      st->skipped += 1;
+      st->good_steps = 0;
+      st->norm = sqrt(sumsq) / S;
+      st->coef = 0.0f;
+      if (st->hysteresis_left > 1) {
+        st->hysteresis_left -= 1;
+      } else {
+        double half = S / 2.0;
+        st->scale = half > c->min_scale ? half : c->min_scale;
+      }
+    } else {
+      double norm = sqrt(sumsq) / S;
+      double clip = 1.0;
+      if (c->max_norm > 0.0) {
+        double q = c->max_norm / (norm + 1e-6);
+        if (q < 1.0) clip = q;
+      }
+      float coef = (float)(clip / S);
+      int64_t t = st->step + 1;
+      orc_scalars s = make_scalars(h, t);
+      /* 3. the update with the scaled and clipped gradient */
+      for (int32_t r = 0; r < N; r++) {
+        if (!((rank_mask >> r) & 1)) continue;
+        for (int64_t j = 0; j < nsegs[r]; j++)
+          for (int64_t e = 0; e < segs[r][4 * nsegs[r] + j]; e++) {
+            int64_t f = segs[r][2 * nsegs[r] + j] + e, i = segs[r][3 * nsegs[r] + j] + e;
+            float g = gbuf[r][i] * coef;
+            adamw_one(&s, g, &master[r][i], &m[r][i], &v[r][i]);
+            uint16_t p16 = to_16(dtype, master[r][i]);
+            if (full16) full16[f] = p16;
+            if (shard16 && shard16[r]) shard16[r][i] = p16;
+          }
+      }
+      st->overflow = 0;
+      st->norm = norm;
+      st->coef = coef;
+      st->step = t;
+      st->good_steps += 1;
+      if (c->window > 0 && st->good_steps >= c->window) {
+        st->scale = S * 2.0;
+        st->good_steps = 0;
+        st->hysteresis_left = c->hysteresis;
+      }
+    }
+  }
+  for (int32_t r = 0; r < N; r++) {
+    free(gbuf[r]);
+    free(segs[r]);
+  }
+  return rc;
+}
