@@ -220,6 +220,83 @@ zero_status zero_step(const zero_plan* plan, const void* const* grads, zero_dtyp
                       void* full_flat16, void* const* out16_shard, const zero_adamw_hparams* hp,
                       int64_t step, uint64_t rank_mask, int64_t bucket_elems, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Mixed-precision controls: dynamic loss scaling, overflow skip, clipping  */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages give these as configuration only ("ZeRO ... 实操" (wmrh.cn) §3.1
+ * and §3.3, ds_config: fp16 loss_scale 0 (dynamic), loss_scale_window,
+ * hysteresis, min_loss_scale; gradient_clipping).  What the library does:
+ *  - the gradient replicas carry the loss scale S; they are reduced as by
+ *    zero_reduce_scatter into binary32 shards, and the squared L2 norm of
+ *    the reduced gradient over every masked rank is accumulated (binary32
+ *    squares, binary64 sums, in a fixed order);
+ *  - a non-finite norm (an inf or NaN anywhere) skips the update: no
+ *    parameter, moment or step count changes; if more than one overflow is
+ *    still tolerated the tolerance drops by one, else S halves (not below
+ *    min_scale); the run of good steps restarts;
+ *  - otherwise norm = sqrt(sumsq)/S; the clip factor is
+ *    min(1, max_norm/(norm + 1e-6)) when max_norm > 0 (as
+ *    torch.nn.utils.clip_grad_norm_), else 1; every element's gradient is
+ *    g * coef with coef = clip/S rounded once to binary32, and AdamW runs as
+ *    zero_adamw_shard_step for step t = state.step + 1, followed by the cast
+ *    and the all-gather of zero_step; after `window` consecutive good steps S
+ *    doubles and the overflow tolerance is restored.
+ * Every decision is taken on the device: no call waits for the host, so a
+ * sequence of steps needs no synchronisation.
+ */
+typedef struct {
+  double init_scale;  /* loss scale of the first gradients (finite, > 0)           */
+  double min_scale;   /* floor of the loss scale (finite, > 0)                       */
+  int32_t window;     /* good steps before the scale doubles; 0 = never grows        */
+  int32_t hysteresis; /* overflows tolerated before the scale halves (>= 1)          */
+  double max_norm;    /* clip threshold of the unscaled global norm; <= 0 = no clip  */
+} zero_amp_config;
+
+/* State of the controls; lives in caller-owned DEVICE memory (16-byte aligned),
+ * written by zero_amp_init and by every zero_step_amp; copy it to the host to
+ * read it. */
+typedef struct {
+  double scale;            /* loss scale the next gradients are expected to carry */
+  double norm;             /* unscaled global L2 norm of the last call (inf/NaN on overflow) */
+  int64_t step;            /* AdamW steps applied (skipped calls not counted)     */
+  int64_t skipped;         /* calls skipped because of a non-finite gradient      */
+  int32_t good_steps;      /* good steps since the scale last changed             */
+  int32_t hysteresis_left; /* overflows still tolerated before the scale halves   */
+  int32_t overflow;        /* 1 if the last call skipped its update               */
+  float coef;              /* gradient multiplier of the last applied update      */
+  float sc[8];             /* binary32 AdamW constants of the last applied update */
+} zero_amp_state;
+
+/* Write the initial state (scale = init_scale, everything else 0, tolerance =
+ * hysteresis) into d_state, asynchronously on `stream`. */
+zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream);
+
+/* Bytes of device workspace zero_step_amp needs for this plan, mask and
+ * bucketing (one binary64 partial sum per 2048-element tile). */
+zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t rank_mask,
+                                     int64_t bucket_elems, int64_t* bytes);
+
+/*
+ * One mixed-precision step (see above).  Arguments as zero_step, plus:
+ *  grad_shards: n_ranks device pointers to float[shard len], written with the
+ *    reduced (still scaled) gradient, the partitioned gradient of ZeRO-2;
+ *  cfg: host pointer, read during the call;
+ *  d_state: the device state (read-modify-write);
+ *  workspace: caller-owned device scratch of at least
+ *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems), 16-byte aligned.
+ * Launches the reduction (one launch per bucket), a one-CTA decision kernel
+ * and the update; calls must not overlap on the device when they share
+ * d_state or workspace.
+ */
+zero_status zero_step_amp(const zero_plan* plan, const void* const* grads, zero_dtype dtype,
+                          zero_reduce_op op, float* const* grad_shards, float* const* master,
+                          float* const* m, float* const* v, void* full_flat16,
+                          void* const* out16_shard, const zero_adamw_hparams* hp,
+                          const zero_amp_config* cfg, void* d_state, void* workspace,
+                          int64_t workspace_bytes, uint64_t rank_mask, int64_t bucket_elems,
+                          void* stream);
+
 /* Synchronize `stream` and report any asynchronous device error. */
 zero_status zero_sync(void* stream);
 

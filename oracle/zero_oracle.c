@@ -494,8 +494,8 @@ int orc_allgather(const int64_t* numel, int32_t n_tensors, int32_t N, int32_t mo
  * 1000, hysteresis 2, min_loss_scale 1; gradient_clipping).  Reading taken:
  *  - the gradients carry the loss scale S; the reduced gradient g (sum or
  *    average of the replicas, as in the plain step) is checked for
- *    non-finite values through its squared norm  sumsq = sum g^2  (binary64,
- *    exact squares);
+ *    non-finite values through its squared norm  sumsq = sum g^2  (each
+ *    square rounded to binary32, the sum taken in binary64);
  *  - non-finite sumsq: the update is skipped (no state, parameter or step
  *    count changes); if more than one overflow is still tolerated the
  *    tolerance drops by one, else S halves (not below min_scale); the
@@ -564,7 +564,8 @@ int orc_step_amp(const int64_t* numel, int32_t n_tensors, int32_t N, int32_t mod
         for (int32_t q = 1; q < N; q++) acc = acc + to_f32(dtype, grads[q][f]);
         if (op == ORC_AVG) acc = acc / (float)N;
         gbuf[r][i] = acc;
-        sumsq += (double)acc * (double)acc;
+        float sq = acc * acc; /* the square is a binary32 number, summed in binary64 */
+        sumsq += (double)sq;
       }
   }
   if (!rc) {

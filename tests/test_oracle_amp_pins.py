@@ -114,7 +114,8 @@ def test_clipping_matches_torch(max_norm):
         opt.step()
         oracle.step_amp(list(w.numel), 1, mode_c, 16, dt, oracle.SUM, g, mst, m, v, full, None, hp,
                         cfg, st)
-        assert abs(st.norm - float(norm)) <= 1e-12 * float(norm)
+        # squares rounded to binary32 (relative error <= 2^-24 each)
+        assert abs(st.norm - float(norm)) <= 2.0 ** -24 * float(norm)
     assert clipped == 3
     ref = p.detach().numpy()
     assert np.max(np.abs(mst[0][:20000] - ref)) <= 1e-6 * np.max(np.abs(ref))

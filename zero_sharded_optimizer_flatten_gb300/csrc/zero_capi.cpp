@@ -135,9 +135,11 @@ void build_jobs(const zero_plan* plan, uint64_t mask, int64_t lo, int64_t hi,
   }
 }
 
-// Launch `kind` over `jobs`, at most kMaxJobs per launch.
+// Launch `kind` over `jobs`, at most kMaxJobs per launch.  `tiles_done`
+// (nullable) numbers the tiles across launches: each launch's first tile is
+// given index *tiles_done (LaunchArgs::tile_base), which then advances.
 zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs& a,
-                        const std::vector<Job>& jobs, void* stream) {
+                        const std::vector<Job>& jobs, void* stream, int64_t* tiles_done) {
   size_t j0 = 0;
   while (j0 < jobs.size()) {
     const size_t nj = std::min<size_t>(jobs.size() - j0, kMaxJobs);
@@ -149,11 +151,13 @@ zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs&
     }
     a.n_jobs = static_cast<int32_t>(nj);
     a.n_tiles = tiles;
+    a.tile_base = tiles_done ? *tiles_done : 0;
     const int err = launch_kernel(kind, dtype, a, stream);
     if (err != 0)
       return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                   cudaGetErrorString(static_cast<cudaError_t>(err)));
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (tiles_done) *tiles_done += tiles;
     j0 += nj;
   }
   return ZERO_OK;
@@ -161,7 +165,8 @@ zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs&
 
 // Run `kind` bucket by bucket over the flat index space.
 zero_status run_buckets(const char* fn, Kind kind, zero_dtype dtype, const zero_plan* plan,
-                        uint64_t mask, int64_t bucket, LaunchArgs& a, void* stream) {
+                        uint64_t mask, int64_t bucket, LaunchArgs& a, void* stream,
+                        int64_t* tiles_done = nullptr) {
   std::vector<Job> jobs;
   const int64_t total = plan->padded;
   const int64_t B = bucket > 0 ? bucket : std::max<int64_t>(total, 1);
@@ -170,9 +175,33 @@ zero_status run_buckets(const char* fn, Kind kind, zero_dtype dtype, const zero_
     const int64_t hi = std::min(total, lo + B);
     build_jobs(plan, mask, lo, hi, jobs);
     if (jobs.empty()) continue;
-    const zero_status st = launch_jobs(fn, kind, dtype, a, jobs, stream);
+    const zero_status st = launch_jobs(fn, kind, dtype, a, jobs, stream, tiles_done);
     if (st != ZERO_OK) return st;
   }
+  return ZERO_OK;
+}
+
+// Tiles run_buckets would launch for this mask and bucketing.
+int64_t count_tiles(const zero_plan* plan, uint64_t mask, int64_t bucket) {
+  std::vector<Job> jobs;
+  const int64_t total = plan->padded;
+  const int64_t B = bucket > 0 ? bucket : std::max<int64_t>(total, 1);
+  int64_t tiles = 0;
+  for (int64_t lo = 0; lo < total; lo += B) {
+    build_jobs(plan, mask, lo, std::min(total, lo + B), jobs);
+    for (const Job& j : jobs) tiles += (j.len + kTile - 1) / kTile;
+  }
+  return tiles;
+}
+
+zero_status check_amp_config(const char* fn, const zero_amp_config* c) {
+  if (!c) return fail(ZERO_ERR_INVALID, "%s: cfg is NULL", fn);
+  if (!isfinite(c->init_scale) || !(c->init_scale > 0) || !isfinite(c->min_scale) ||
+      !(c->min_scale > 0))
+    return fail(ZERO_ERR_INVALID, "%s: init_scale and min_scale must be finite and > 0", fn);
+  if (c->window < 0 || c->hysteresis < 1)
+    return fail(ZERO_ERR_INVALID, "%s: need window >= 0 and hysteresis >= 1", fn);
+  if (!isfinite(c->max_norm)) return fail(ZERO_ERR_INVALID, "%s: max_norm must be finite", fn);
   return ZERO_OK;
 }
 
@@ -342,6 +371,99 @@ extern "C" zero_status zero_step(const zero_plan* plan, const void* const* grads
   a.sc = make_scalars(*hp, step);
   set_scale(a, plan->n_ranks, op);
   return run_buckets(fn, Kind::kStep, dtype, plan, rank_mask, bucket_elems, a, stream);
+}
+
+extern "C" zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream) {
+  const char* fn = "zero_amp_init";
+  clear_error();
+  ZERO_TRY(check_amp_config(fn, cfg));
+  if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
+  if (!aligned16(d_state)) return fail(ZERO_ERR_ALIGN, "%s: d_state is not 16-byte aligned", fn);
+  ZERO_TRY(pending_error(fn));
+  zero_amp_state init;
+  memset(&init, 0, sizeof init);
+  init.scale = cfg->init_scale;
+  init.hysteresis_left = cfg->hysteresis;
+  init.coef = 1.0f;
+  const int err = launch_amp_init(static_cast<zero_amp_state*>(d_state), init, stream);
+  if (err != 0)
+    return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
+                cudaGetErrorString(static_cast<cudaError_t>(err)));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return ZERO_OK;
+}
+
+extern "C" zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t rank_mask,
+                                                int64_t bucket_elems, int64_t* bytes) {
+  const char* fn = "zero_amp_workspace_bytes";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  if (!bytes) return fail(ZERO_ERR_INVALID, "%s: bytes is NULL", fn);
+  *bytes = count_tiles(plan, rank_mask, bucket_elems) * static_cast<int64_t>(sizeof(double));
+  return ZERO_OK;
+}
+
+extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* grads,
+                                     zero_dtype dtype, zero_reduce_op op,
+                                     float* const* grad_shards, float* const* master,
+                                     float* const* m, float* const* v, void* full_flat16,
+                                     void* const* out16_shard, const zero_adamw_hparams* hp,
+                                     const zero_amp_config* cfg, void* d_state, void* workspace,
+                                     int64_t workspace_bytes, uint64_t rank_mask,
+                                     int64_t bucket_elems, void* stream) {
+  const char* fn = "zero_step_amp";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, 1));
+  ZERO_TRY(check_amp_config(fn, cfg));
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  if (out16_shard) ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, true));
+  if (full_flat16 && !aligned16(full_flat16))
+    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
+  if (!aligned16(d_state)) return fail(ZERO_ERR_ALIGN, "%s: d_state is not 16-byte aligned", fn);
+  const int64_t tiles = count_tiles(plan, rank_mask, bucket_elems);
+  const int64_t need = tiles * static_cast<int64_t>(sizeof(double));
+  if (!workspace) return fail(ZERO_ERR_INVALID, "%s: workspace is NULL", fn);
+  if (!aligned16(workspace)) return fail(ZERO_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
+  if (workspace_bytes < need)
+    return fail(ZERO_ERR_INVALID, "%s: workspace holds %" PRId64 " bytes, needs %" PRId64, fn,
+                workspace_bytes, need);
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (!in_mask(rank_mask, r)) continue;
+    a.gshard[r] = grad_shards[r];
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+    a.shard16[r] = out16_shard ? out16_shard[r] : nullptr;
+  }
+  a.full16 = full_flat16;
+  a.partials = static_cast<double*>(workspace);
+  a.amp = static_cast<const zero_amp_state*>(d_state);
+  set_scale(a, plan->n_ranks, op);
+  int64_t done = 0;
+  ZERO_TRY(run_buckets(fn, Kind::kStats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
+  AmpParams p;
+  p.cfg = *cfg;
+  p.hp = *hp;
+  const int err = launch_amp_finalize(a.partials, done, static_cast<zero_amp_state*>(d_state), p,
+                                      stream);
+  if (err != 0)
+    return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
+                cudaGetErrorString(static_cast<cudaError_t>(err)));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return run_buckets(fn, Kind::kAdamwAmp, dtype, plan, rank_mask, 0, a, stream);
 }
 
 extern "C" zero_status zero_sync(void* stream) {

@@ -75,10 +75,24 @@ struct LaunchArgs {
   int32_t n_jobs;
   int32_t pad_;
   int64_t n_tiles;
+  double* partials;                // mixed-precision: per-tile binary64 sums of squares
+  int64_t tile_base;               // index of this launch's first tile among the step's
+  const zero_amp_state* amp;       // mixed-precision: device state of the controls
   Job jobs[kMaxJobs];
 };
 
-enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit };
+enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kAdamwAmp };
+
+// Parameters of the one-CTA decision kernel of the mixed-precision step.
+struct AmpParams {
+  zero_amp_config cfg;
+  zero_adamw_hparams hp;
+};
+
+// Host launchers of the mixed-precision helpers (zero_launch.cu).
+int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
+                        const AmpParams& p, void* stream);
+int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream);
 
 // Host launcher entry (zero_kernels_*.cu): launches `kind` for the jobs in
 // `a` on `stream`; returns a CUDA error code (0 on success).

@@ -396,6 +396,110 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_init(const __grid
 }
 
 // ---------------------------------------------------------------------------
+// mixed-precision controls
+
+// Sum of x over the block in binary64, in a fixed order (shuffle tree inside
+// each warp, then the warps in index order); the result is valid in thread 0.
+template <int NT>
+__device__ __forceinline__ double block_sum(double x) {
+  __shared__ double warp_part[NT / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_part[warp] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < NT / 32; ++w) t += warp_part[w];
+  __syncthreads();
+  return t;
+}
+
+// Reduce-scatter into fp32 shards plus, per tile, the binary64 sum of the
+// binary32 squares of the reduced gradient (a thread adds its up to 8
+// squares in binary32 first).  A non-finite gradient makes the sum non-finite.
+template <class T, int NR>
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
+  for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+    const Job& jb = a.jobs[find_job(a, tile)];
+    const int64_t base = (tile - jb.tile_begin) * kTile;
+    float s = 0.f;
+    if (jb.vec) {
+      const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
+      if (e0 < jb.len) {
+        const bool two = e0 + kHalf < jb.len;
+        const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
+        float g[8];
+        reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
+        store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s = __fadd_rn(s, __fmul_rn(g[k], g[k]));
+      }
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < kTile / kThreads; ++k) {
+        const int64_t e = base + k * kThreads + threadIdx.x;
+        if (e < jb.len) {
+          const float g = reduce1<T, NR>(a, jb.flat_off + e);
+          a.gshard[jb.rank][jb.shard_off + e] = g;
+          s = __fadd_rn(s, __fmul_rn(g, g));
+        }
+      }
+    }
+    const double t = block_sum<kThreads>(static_cast<double>(s));
+    if (threadIdx.x == 0) a.partials[a.tile_base + tile] = t;
+  }
+}
+
+// AdamW + cast + all-gather on the reduced fp32 gradient times the decision
+// kernel's coefficient; does nothing when the decision was to skip.
+template <class T>
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw_amp(const __grid_constant__ LaunchArgs a) {
+  if (__ldcg(&a.amp->overflow) != 0) return;
+  const float coef = __ldcg(&a.amp->coef);
+  StepScalars sc;
+  sc.d = __ldcg(&a.amp->sc[0]);
+  sc.b1 = __ldcg(&a.amp->sc[1]);
+  sc.b2 = __ldcg(&a.amp->sc[2]);
+  sc.c1 = __ldcg(&a.amp->sc[3]);
+  sc.c2 = __ldcg(&a.amp->sc[4]);
+  sc.ss = __ldcg(&a.amp->sc[5]);
+  sc.sb = __ldcg(&a.amp->sc[6]);
+  sc.eps = __ldcg(&a.amp->sc[7]);
+  for_each_tile(
+      a,
+      [&](const Job& jb, int64_t e0, bool two) {
+        const int r = jb.rank;
+        const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
+        const int64_t f1 = f0 + kHalf, i1 = i0 + kHalf;
+        float g[8], p[8], m[8], v[8];
+        load_state2(a.gshard[r], i0, i1, two, g);
+        load_state2(a.master[r], i0, i1, two, p);
+        load_state2(a.m[r], i0, i1, two, m);
+        load_state2(a.v[r], i0, i1, two, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) adamw1(sc, __fmul_rn(g[k], coef), p[k], m[k], v[k]);
+        store_state2(a.master[r], i0, i1, two, p);
+        store_state2(a.m[r], i0, i1, two, m);
+        store_state2(a.v[r], i0, i1, two, v);
+        if (a.full16) store_16x2<T>(a.full16, f0, f1, two, p);
+        if (a.shard16[r]) store_16x2<T>(a.shard16[r], i0, i1, two, p);
+      },
+      [&](const Job& jb, int64_t e) {
+        const int64_t f = jb.flat_off + e, i = jb.shard_off + e;
+        const int r = jb.rank;
+        float p = a.master[r][i], m = a.m[r][i], v = a.v[r][i];
+        adamw1(sc, __fmul_rn(a.gshard[r][i], coef), p, m, v);
+        a.master[r][i] = p;
+        a.m[r][i] = m;
+        a.v[r][i] = v;
+        const uint16_t o = Fmt<T>::narrow(p);
+        if (a.full16) static_cast<uint16_t*>(a.full16)[f] = o;
+        if (a.shard16[r]) static_cast<uint16_t*>(a.shard16[r])[i] = o;
+      });
+}
+
+// ---------------------------------------------------------------------------
 // launch (host)
 
 // Grid of a launch of kernel `fn` over n_tiles tiles (see ZERO_GRID_MULT).
@@ -426,6 +530,11 @@ struct PickReduce {
   static const void* get() { return reinterpret_cast<const void*>(&k_reduce_scatter<T, NR>); }
 };
 
+template <class T, int NR>
+struct PickStats {
+  static const void* get() { return reinterpret_cast<const void*>(&k_stats<T, NR>); }
+};
+
 template <class T>
 int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
   const void* fn = nullptr;
@@ -435,6 +544,8 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kAdamw: fn = reinterpret_cast<const void*>(&k_adamw<T>); break;
     case Kind::kAllgather: fn = reinterpret_cast<const void*>(&k_allgather<T>); break;
     case Kind::kInit: fn = reinterpret_cast<const void*>(&k_init<T>); break;
+    case Kind::kStats: fn = by_ranks<T, PickStats>(a.n_ranks); break;
+    case Kind::kAdamwAmp: fn = reinterpret_cast<const void*>(&k_adamw_amp<T>); break;
   }
   const int grid = grid_for(fn, a.n_tiles);
   if (grid <= 0) return static_cast<int>(cudaGetLastError());

@@ -38,6 +38,76 @@ int grid_for(const void* fn, int64_t n_tiles) {
   return static_cast<int>(n_tiles < slots ? n_tiles : slots);
 }
 
+// The decision of the mixed-precision step (one CTA): sum the per-tile
+// partials in a fixed order, then update the loss-scale state and form the
+// step's coefficient and AdamW constants (binary64, each rounded once).
+constexpr int kFinalizeThreads = 1024;
+
+__global__ void __launch_bounds__(kFinalizeThreads) k_amp_finalize(const double* partials,
+                                                                   int64_t n,
+                                                                   zero_amp_state* st,
+                                                                   const AmpParams p) {
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += kFinalizeThreads) s += __ldcg(partials + i);
+  const double sumsq = block_sum<kFinalizeThreads>(s);
+  if (threadIdx.x != 0) return;
+  zero_amp_state x = *st;
+  const double S = x.scale;
+  x.norm = sqrt(sumsq) / S;
+  if (!isfinite(sumsq)) {
+    x.overflow = 1;
+    x.skipped += 1;
+    x.good_steps = 0;
+    x.coef = 0.0f;
+    if (x.hysteresis_left > 1) {
+      x.hysteresis_left -= 1;
+    } else {
+      const double half = S / 2.0;
+      x.scale = half > p.cfg.min_scale ? half : p.cfg.min_scale;
+    }
+  } else {
+    double clip = 1.0;
+    if (p.cfg.max_norm > 0.0) {
+      const double q = p.cfg.max_norm / (x.norm + 1e-6);
+      if (q < 1.0) clip = q;
+    }
+    x.coef = static_cast<float>(clip / S);
+    const int64_t t = x.step + 1;
+    const zero_adamw_hparams& h = p.hp;
+    x.sc[0] = static_cast<float>(1.0 - h.lr * h.weight_decay);
+    x.sc[1] = static_cast<float>(h.beta1);
+    x.sc[2] = static_cast<float>(h.beta2);
+    x.sc[3] = static_cast<float>(1.0 - h.beta1);
+    x.sc[4] = static_cast<float>(1.0 - h.beta2);
+    x.sc[5] = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
+    x.sc[6] = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
+    x.sc[7] = static_cast<float>(h.eps);
+    x.overflow = 0;
+    x.step = t;
+    x.good_steps += 1;
+    if (p.cfg.window > 0 && x.good_steps >= p.cfg.window) {
+      x.scale = S * 2.0;
+      x.good_steps = 0;
+      x.hysteresis_left = p.cfg.hysteresis;
+    }
+  }
+  *st = x;
+}
+
+__global__ void k_amp_init(zero_amp_state* st, const zero_amp_state v) { *st = v; }
+
+int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
+                        const AmpParams& p, void* stream) {
+  k_amp_finalize<<<1, kFinalizeThreads, 0, static_cast<cudaStream_t>(stream)>>>(partials, n_tiles,
+                                                                               state, p);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream) {
+  k_amp_init<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(state, init);
+  return static_cast<int>(cudaGetLastError());
+}
+
 int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == ZERO_BF16) return launch_typed<__nv_bfloat16>(kind, a, s);
