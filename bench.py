@@ -288,7 +288,7 @@ class FlatRunner:
     (bucketed if the workload says so).  Gradient buffers hold only the flat
     range the masked ranks own."""
 
-    def __init__(self, w, dev, grad_sets):
+    def __init__(self, w, dev, grad_sets, amp=None):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
@@ -308,13 +308,32 @@ class FlatRunner:
         del p16
         self.grads = [[W.grads16(w, s + 1, q, dev, 0, ext) for q in range(w.n_ranks)]
                       for s in range(grad_sets)]
-        self.calls = [Z.ZeroStep(plan, g, w.op, self.master, self.m, self.v, self.full16, None,
-                                 self.hp, rank_mask=self.mask, bucket_elems=w.bucket_elems)
-                      for g in self.grads]
         self.elems = sum(S)                       # work units per step
         self.padded = plan.padded
-        self.bytes_per_step = step_bytes(self.elems, w.n_ranks)
-        self.kernel = KERNEL_PREFIX
+        if amp is None:
+            self.calls = [Z.ZeroStep(plan, g, w.op, self.master, self.m, self.v, self.full16,
+                                     None, self.hp, rank_mask=self.mask,
+                                     bucket_elems=w.bucket_elems) for g in self.grads]
+            self.bytes_per_step = step_bytes(self.elems, w.n_ranks)
+            self.kernel = KERNEL_PREFIX
+        else:
+            # mixed-precision controls: fp32 gradient shards, device state, workspace
+            self.gsh = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+            self.state = Z.amp_state_tensor(dev)
+            Z.zero_amp_init(self.state, amp)
+            self.ws = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan, self.mask,
+                                                                      w.bucket_elems)),
+                                  dtype=torch.uint8, device=dev)
+
+            def make(g):
+                return lambda t: Z.zero_step_amp(plan, g, w.op, self.gsh, self.master, self.m,
+                                                 self.v, self.full16, None, self.hp, amp,
+                                                 self.state, self.ws, rank_mask=self.mask,
+                                                 bucket_elems=w.bucket_elems)
+            self.calls = [make(g) for g in self.grads]
+            # reduction pass 2N + 4 B, update pass 4 + 24 + 2 B per element
+            self.bytes_per_step = (2 * w.n_ranks + 34) * self.elems
+            self.kernel = "k_stats + k_amp_finalize + k_adamw_amp"
 
     def step(self, t, events=None):
         if events is not None:
@@ -420,7 +439,11 @@ def run_gpu(args, world, rank, local):
     if w.zero3:
         run = Zero3Runner(w, dev, args.layer_states)
     else:
-        run = FlatRunner(w, dev, args.grad_sets)
+        amp = None
+        if args.amp:
+            amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
+                              max_norm=args.max_norm)
+        run = FlatRunner(w, dev, args.grad_sets, amp)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -466,7 +489,7 @@ def run_gpu(args, world, rank, local):
         bytes_per_launch = run.bytes_per_step
 
     e2e = None
-    if not w.zero3:
+    if not w.zero3 and not args.amp:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         e2e_s, h2d, d2h = run.e2e(t, e2e_steps)
         e2e_s = max_over_ranks(dist, e2e_s, local)
@@ -515,6 +538,9 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks.summary(wall0, wall1),
     }
+    if args.amp:
+        line["config"]["amp"] = {"max_norm": args.max_norm, "init_scale": 1.0,
+                                 "note": "loss-scale check, global-norm clipping, skip on overflow"}
     if w.zero3:
         line["config"]["layer_states"] = run.n_states
         line["config"]["layers"] = run.layers
@@ -543,6 +569,9 @@ def main(argv=None):
                     help="parameter group to time (the reported line uses the default)")
     ap.add_argument("--grad-sets", type=int, default=2,
                     help="distinct gradient sets resident in HBM, alternated per step")
+    ap.add_argument("--amp", action="store_true",
+                    help="time the mixed-precision step (norm check + clipping) instead")
+    ap.add_argument("--max-norm", type=float, default=1.0)
     ap.add_argument("--layer-states", type=int, default=40,
                     help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")
     args = ap.parse_args(argv)

@@ -1,0 +1,215 @@
+"""Parity of the mixed-precision step (loss scaling, overflow skip, global-norm
+clipping) between the CUDA path and the oracle.
+
+The norm is accumulated in a different order on the two sides (per-tile
+binary64 sums against one flat binary64 sum), so the clip coefficient may
+differ in its last bit when clipping is active; the state's integer fields,
+the loss scale and every skip decision must agree exactly, the norm to 1e-6
+relative, the coefficient to 1 ulp, and the buffers to the usual bar.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._harness import (Case, assert_16_close, assert_fp32_close, dt_code, f32, hp_oracle,
+                            mode_code, op_code, owner_of, sample_indices, u16)
+from zero_sharded_optimizer_flatten_gb300 import workloads as W
+from zero_sharded_optimizer_flatten_gb300 import zero as Z
+
+pytestmark = pytest.mark.gpu
+
+HP = Z.AdamW()
+
+
+@pytest.fixture(autouse=True)
+def _cuda_cleanup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _ocfg(c: Z.AmpConfig):
+    return oracle.amp_config(c.init_scale, c.min_scale, c.window, c.hysteresis, c.max_norm)
+
+
+class AmpCase(Case):
+    def __init__(self, w, cfg: Z.AmpConfig, bucket=0, with_oracle=True):
+        super().__init__(w, with_oracle=with_oracle)
+        self.cfg, self.bucket = cfg, bucket
+        self.gsh = [torch.empty(self.plan.shard_len(r) if (w.mask >> r) & 1 else 0,
+                                dtype=torch.float32, device="cuda") for r in range(w.n_ranks)]
+        self.state = Z.amp_state_tensor()
+        Z.zero_amp_init(self.state, cfg)
+        nbytes = Z.zero_amp_workspace_bytes(self.plan, w.mask, bucket)
+        self.ws = torch.empty(max(16, nbytes), dtype=torch.uint8, device="cuda")
+        self.ost = oracle.amp_init(_ocfg(cfg)) if with_oracle else None
+
+    def grads_scaled(self, t, scale):
+        return [W.grads16(self.w, t, q, "cuda", scale=scale) for q in range(self.w.n_ranks)]
+
+    def gpu_step(self, g):
+        Z.zero_step_amp(self.plan, g, self.w.op, self.gsh, self.master, self.m, self.v,
+                        self.full16, None, HP, self.cfg, self.state, self.ws,
+                        rank_mask=self.w.mask, bucket_elems=self.bucket)
+
+    def oracle_step_amp(self, g):
+        w = self.w
+        oracle.step_amp(list(w.numel), w.n_ranks, mode_code(w), w.align, dt_code(w), op_code(w),
+                        [u16(x) for x in g], self.o_master, self.o_m, self.o_v, self.o_full, None,
+                        hp_oracle(HP), _ocfg(self.cfg), self.ost, w.mask)
+
+    def compare_state(self, what):
+        s = Z.read_amp_state(self.state)
+        o = self.ost
+        assert (s.step, s.skipped, s.good_steps, s.hysteresis_left, s.overflow) == \
+            (o.step, o.skipped, o.good_steps, o.hysteresis_left, o.overflow), what
+        assert s.scale == o.scale, what
+        if o.overflow:
+            assert not np.isfinite(s.norm), what
+        else:
+            assert abs(s.norm - o.norm) <= 1e-6 * abs(o.norm), (what, s.norm, o.norm)
+            d = abs(int(np.float32(s.coef).view(np.int32)) - int(np.float32(o.coef).view(np.int32)))
+            assert d <= 1, (what, s.coef, o.coef)
+        return s
+
+
+CASES = [
+    # numel, N, mode, A, dtype, op, cfg
+    ((1000, 37, 4096, 3, 129), 4, "flat", 16, "fp16", "avg",
+     Z.AmpConfig(init_scale=1024.0, window=3, hysteresis=2, max_norm=0.0)),
+    ((1000, 37, 4096, 3, 129), 4, "flat", 16, "fp16", "sum",
+     Z.AmpConfig(init_scale=256.0, window=1000, hysteresis=1, max_norm=0.05)),
+    ((1000, 37, 4096, 3, 129), 3, "round_robin", 1, "bf16", "avg",
+     Z.AmpConfig(init_scale=1.0, window=0, hysteresis=1, max_norm=0.01)),
+    ((70001,), 8, "flat", 2, "bf16", "avg",
+     Z.AmpConfig(init_scale=8.0, window=2, hysteresis=1, max_norm=0.02)),
+]
+
+
+@pytest.mark.parametrize("numel,N,mode,A,dtype,op,cfg", CASES)
+def test_amp_small_groups(numel, N, mode, A, dtype, op, cfg):
+    w = W.small(numel, N, mode=mode, align=A, dtype=dtype, op=op, outlier_frac=0.01)
+    c = AmpCase(w, cfg)
+    for t in range(1, 5):
+        g = c.grads_scaled(t, c.ost.scale)
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        c.compare_state(f"step {t}")
+        c.compare(f"amp step {t}")
+
+
+def test_amp_overflow_trajectory():
+    """A loss scale of 2^20 overflows fp16 gradients: the steps are skipped and
+    the scale falls until the gradients fit, then updates resume."""
+    w = W.small((3000, 129, 4096), 4, mode="flat", align=16, dtype="fp16", op="avg")
+    cfg = Z.AmpConfig(init_scale=2.0 ** 20, min_scale=1.0, window=4, hysteresis=2)
+    c = AmpCase(w, cfg)
+    seen_skip = seen_step = False
+    for t in range(1, 13):
+        g = c.grads_scaled(t, c.ost.scale)
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        s = c.compare_state(f"call {t}")
+        seen_skip |= bool(s.overflow)
+        seen_step |= not s.overflow
+        c.compare(f"call {t}")
+    assert seen_skip and seen_step
+
+
+def test_amp_skip_leaves_buffers_untouched():
+    w = W.small((5000, 33), 2, mode="flat", align=16, dtype="fp16", op="sum")
+    c = AmpCase(w, Z.AmpConfig(init_scale=4.0, hysteresis=1))
+    g = c.grads_scaled(1, 4.0)
+    c.gpu_step(g)
+    torch.cuda.synchronize()
+    before = [x.clone() for x in c.master + c.m + c.v] + [c.full16.clone()]
+    g = c.grads_scaled(2, 4.0)
+    g[1][777] = float("nan")
+    c.gpu_step(g)
+    torch.cuda.synchronize()
+    s = Z.read_amp_state(c.state)
+    assert s.overflow == 1 and s.step == 1 and s.skipped == 1 and s.scale == 2.0
+    after = [x for x in c.master + c.m + c.v] + [c.full16]
+    for a, b in zip(before, after):
+        assert torch.equal(a, b)
+
+
+def test_amp_unit_scale_is_the_fused_step():
+    """S = 1 and no clipping: bit-identical to zero_step."""
+    w = W.small((20000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    c = AmpCase(w, Z.AmpConfig(init_scale=1.0, window=0, hysteresis=1), with_oracle=False)
+    ref = Case(w, with_oracle=False)
+    for t in (1, 2, 3):
+        g = c.grads_scaled(t, 1.0)
+        c.gpu_step(g)
+        Z.zero_step(ref.plan, g, "avg", ref.master, ref.m, ref.v, ref.full16, None, HP, t)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(c.master[r], ref.master[r]) and torch.equal(c.v[r], ref.v[r])
+    assert torch.equal(c.full16, ref.full16)
+
+
+@pytest.mark.parametrize("bucket", [1000, 4096])
+def test_amp_buckets(bucket):
+    w = W.small((30000, 37, 4096), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    cfg = Z.AmpConfig(init_scale=1.0, window=0, hysteresis=1, max_norm=0.0)
+    a = AmpCase(w, cfg, with_oracle=False)
+    b = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    for t in (1, 2):
+        g = a.grads_scaled(t, 1.0)
+        a.gpu_step(g)
+        b.gpu_step(g)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(a.master[r], b.master[r])
+    sa, sb = Z.read_amp_state(a.state), Z.read_amp_state(b.state)
+    # the tiles (and so the summation grouping) follow the buckets
+    assert abs(sa.norm - sb.norm) <= 1e-6 * sa.norm
+
+
+def test_amp_workspace_too_small_is_rejected():
+    w = W.small((30000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
+    c = AmpCase(w, Z.AmpConfig(), with_oracle=False)
+    small = c.ws[:8]
+    before = Z.zero_launch_count()
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_step_amp(c.plan, c.grads_scaled(1, 1.0), "avg", c.gsh, c.master, c.m, c.v,
+                        c.full16, None, HP, c.cfg, c.state, small)
+    assert e.value.status == Z.ZERO_ERR_INVALID and Z.zero_launch_count() == before
+
+
+def test_amp_toy_model_full_size():
+    """The round-robin ToyModel group (100.7M, fp16, N=4, summed, 1 % outliers)
+    with DeepSpeed-like controls: scale 2^16, window 2, hysteresis 2,
+    clipping at 1.0.  The oracle runs the whole group (the norm is global);
+    the buffers are compared on sampled elements."""
+    w = W.WORKLOADS["toy_rr"]
+    cfg = Z.AmpConfig(init_scale=65536.0, min_scale=1.0, window=2, hysteresis=2, max_norm=1.0)
+    c = AmpCase(w, cfg)
+    F = sample_indices(w, n_random=20000)
+    rank, shard = owner_of(w, F)
+    applied = 0
+    for t in range(1, 9):
+        g = c.grads_scaled(t, c.ost.scale)
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        applied += not c.compare_state(f"call {t}").overflow
+        del g
+    assert applied >= 2
+    for r in range(w.n_ranks):
+        sel = rank == r
+        it = torch.from_numpy(shard[sel]).cuda()
+        assert_fp32_close(f32(c.master[r][it]), c.o_master[r][shard[sel]], f"master[{r}]")
+        assert_fp32_close(f32(c.m[r][it]), c.o_m[r][shard[sel]], f"m[{r}]")
+        assert_fp32_close(f32(c.v[r][it]), c.o_v[r][shard[sel]], f"v[{r}]")
+    Ft = torch.from_numpy(F).cuda()
+    assert_16_close(u16(c.full16[Ft]), c.o_full[F], "full16")

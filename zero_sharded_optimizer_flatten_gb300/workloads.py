@@ -151,7 +151,7 @@ def _seed(*parts) -> int:
 
 
 def _chunk(w: Workload, kind: str, step: int, rank: int, c: int, n: int, sigma: float,
-           device) -> torch.Tensor:
+           device, scale: float = 1.0) -> torch.Tensor:
     gen = torch.Generator(device=device)
     gen.manual_seed(_seed(w.seed, kind, step, rank, c))
     x = torch.randn(n, generator=gen, device=device, dtype=torch.float32)
@@ -159,15 +159,19 @@ def _chunk(w: Workload, kind: str, step: int, rank: int, c: int, n: int, sigma: 
     if kind == "grad" and w.outlier_frac > 0:
         hit = torch.rand(n, generator=gen, device=device, dtype=torch.float32) < w.outlier_frac
         x = torch.where(hit, x * w.outlier_scale, x)
+    if scale != 1.0:
+        x.mul_(scale)
     return x.to(w.torch_dtype)
 
 
 def fill(w: Workload, kind: str, step: int, rank: int, lo: int, hi: int, out: torch.Tensor,
-         layer: int = 0) -> torch.Tensor:
+         layer: int = 0, scale: float = 1.0) -> torch.Tensor:
     """Write the seeded values of flat range [lo, hi) into ``out`` (length hi-lo).
 
     kind "param": the initial 16-bit parameters (sigma = param_sigma);
-    kind "grad": rank `rank`'s gradient replica at `step` (sigma = grad_sigma).
+    kind "grad": rank `rank`'s gradient replica at `step` (sigma = grad_sigma),
+    multiplied by `scale` (a loss scale the backward pass would carry) before
+    the rounding to 16 bits, so large scales overflow to infinity.
     Elements at or beyond phi (the tail padding) are zero.
     """
     assert out.numel() == hi - lo and out.dtype == w.torch_dtype
@@ -182,7 +186,7 @@ def fill(w: Workload, kind: str, step: int, rank: int, lo: int, hi: int, out: to
         a, b = max(c0, lo), min(c1, real_hi)
         if a < b:
             vals = _chunk(w, kind, step, rank if kind == "grad" else -1, (layer, c), c1 - c0,
-                          sigma, dev)
+                          sigma, dev, scale)
             out[a - lo:b - lo].copy_(vals[a - c0:b - c0])
         c += 1
     return out
@@ -194,10 +198,10 @@ def params16(w: Workload, device, layer: int = 0) -> torch.Tensor:
 
 
 def grads16(w: Workload, step: int, rank: int, device, lo: int = 0, hi: Optional[int] = None,
-            layer: int = 0) -> torch.Tensor:
+            layer: int = 0, scale: float = 1.0) -> torch.Tensor:
     hi = flat_len(w) if hi is None else hi
     return fill(w, "grad", step, rank, lo, hi,
-                torch.empty(hi - lo, dtype=w.torch_dtype, device=device), layer)
+                torch.empty(hi - lo, dtype=w.torch_dtype, device=device), layer, scale)
 
 
 def small(numel, n_ranks, mode="flat", align=16, dtype="fp16", op="avg", grad_sigma=1e-2,

@@ -405,3 +405,107 @@ class ZeroStep:
         _check(lib().zero_step(self.plan.handle, self._g, self.dt, self.op, self._ms, self._mm,
                                self._vv, self._full, self._o16, ctypes.byref(self._hp),
                                int(step), self.mask, self.bucket, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# mixed-precision controls
+
+
+class AmpConfigC(ctypes.Structure):
+    _fields_ = [("init_scale", ctypes.c_double), ("min_scale", ctypes.c_double),
+                ("window", ctypes.c_int32), ("hysteresis", ctypes.c_int32),
+                ("max_norm", ctypes.c_double)]
+
+
+class AmpState(ctypes.Structure):
+    """Host image of zero_amp_state (80 bytes)."""
+    _fields_ = [("scale", ctypes.c_double), ("norm", ctypes.c_double),
+                ("step", ctypes.c_int64), ("skipped", ctypes.c_int64),
+                ("good_steps", ctypes.c_int32), ("hysteresis_left", ctypes.c_int32),
+                ("overflow", ctypes.c_int32), ("coef", ctypes.c_float),
+                ("sc", ctypes.c_float * 8)]
+
+
+AMP_STATE_BYTES = ctypes.sizeof(AmpState)
+
+
+@dataclasses.dataclass
+class AmpConfig:
+    init_scale: float = 65536.0
+    min_scale: float = 1.0
+    window: int = 1000
+    hysteresis: int = 2
+    max_norm: float = 0.0
+
+    def c(self) -> AmpConfigC:
+        return AmpConfigC(self.init_scale, self.min_scale, self.window, self.hysteresis,
+                          self.max_norm)
+
+
+def amp_state_tensor(device="cuda"):
+    """Device buffer for a zero_amp_state (torch allocations are 256-byte aligned)."""
+    torch = _torch()
+    return torch.zeros(AMP_STATE_BYTES, dtype=torch.uint8, device=device)
+
+
+def read_amp_state(d_state) -> AmpState:
+    """Copy the device state to the host (synchronizes with the current stream)."""
+    raw = d_state.detach().cpu().numpy().tobytes()
+    return AmpState.from_buffer_copy(raw)
+
+
+def zero_amp_init(d_state, cfg: AmpConfig, stream=None):
+    L = lib()
+    L.zero_amp_init.argtypes = [ctypes.c_void_p, ctypes.POINTER(AmpConfigC), ctypes.c_void_p]
+    L.zero_amp_init.restype = ctypes.c_int
+    c = cfg.c()
+    _check(L.zero_amp_init(_addr(d_state, "d_state", AMP_STATE_BYTES), ctypes.byref(c),
+                           _stream(stream)))
+
+
+def zero_amp_workspace_bytes(plan: Plan, rank_mask=None, bucket_elems=0) -> int:
+    L = lib()
+    L.zero_amp_workspace_bytes.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int64,
+                                           ctypes.POINTER(ctypes.c_int64)]
+    L.zero_amp_workspace_bytes.restype = ctypes.c_int
+    out = ctypes.c_int64()
+    _check(L.zero_amp_workspace_bytes(plan.handle, _mask(plan, rank_mask), int(bucket_elems),
+                                      ctypes.byref(out)))
+    return out.value
+
+
+def zero_step_amp(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16, out16_shard,
+                  hparams: AdamW, cfg: AmpConfig, d_state, workspace, rank_mask=None,
+                  bucket_elems=0, stream=None, dtype=None):
+    """Mixed-precision step: loss-scale check, clipping, AdamW, cast, gather."""
+    torch = _torch()
+    L = lib()
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    L.zero_step_amp.argtypes = [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp, vp, vpp,
+                                ctypes.POINTER(AdamWHparams), ctypes.POINTER(AmpConfigC), vp, vp,
+                                ctypes.c_int64, ctypes.c_uint64, ctypes.c_int64, vp]
+    L.zero_step_amp.restype = ctypes.c_int
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    o16 = (_ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+           if out16_shard is not None else None)
+    need = zero_amp_workspace_bytes(plan, mask, bucket_elems)
+    ws_bytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) \
+        else need
+    ws = _addr(workspace, "workspace")
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    hp = hparams.c()
+    c = cfg.c()
+    _check(L.zero_step_amp(plan.handle, _ptrs(g), dt, op_i, _ptrs(gs), _ptrs(ms), _ptrs(mm),
+                           _ptrs(vv), full, o16, ctypes.byref(hp), ctypes.byref(c),
+                           _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
+                           int(bucket_elems), _stream(stream)))
