@@ -273,7 +273,8 @@ typedef struct {
 zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream);
 
 /* Bytes of device workspace zero_step_amp needs for this plan, mask and
- * bucketing (one binary64 partial sum per 2048-element tile). */
+ * bucketing: 4 KB of copies of the step's decision record plus one binary64
+ * partial sum per 2048-element tile. */
 zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t rank_mask,
                                      int64_t bucket_elems, int64_t* bytes);
 

@@ -399,7 +399,8 @@ extern "C" zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t 
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   if (!bytes) return fail(ZERO_ERR_INVALID, "%s: bytes is NULL", fn);
-  *bytes = count_tiles(plan, rank_mask, bucket_elems) * static_cast<int64_t>(sizeof(double));
+  *bytes = kAmpBcastBytes + count_tiles(plan, rank_mask, bucket_elems) *
+                                static_cast<int64_t>(sizeof(double));
   return ZERO_OK;
 }
 
@@ -429,7 +430,7 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
   if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
   if (!aligned16(d_state)) return fail(ZERO_ERR_ALIGN, "%s: d_state is not 16-byte aligned", fn);
   const int64_t tiles = count_tiles(plan, rank_mask, bucket_elems);
-  const int64_t need = tiles * static_cast<int64_t>(sizeof(double));
+  const int64_t need = kAmpBcastBytes + tiles * static_cast<int64_t>(sizeof(double));
   if (!workspace) return fail(ZERO_ERR_INVALID, "%s: workspace is NULL", fn);
   if (!aligned16(workspace)) return fail(ZERO_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
   if (workspace_bytes < need)
@@ -449,16 +450,18 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
     a.shard16[r] = out16_shard ? out16_shard[r] : nullptr;
   }
   a.full16 = full_flat16;
-  a.partials = static_cast<double*>(workspace);
-  a.amp = static_cast<const zero_amp_state*>(d_state);
+  // workspace: [decision record copies][one binary64 partial per tile]
+  AmpBcast* bcast = static_cast<AmpBcast*>(workspace);
+  a.bcast = bcast;
+  a.partials = reinterpret_cast<double*>(static_cast<char*>(workspace) + kAmpBcastBytes);
   set_scale(a, plan->n_ranks, op);
   int64_t done = 0;
   ZERO_TRY(run_buckets(fn, Kind::kStats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
   AmpParams p;
   p.cfg = *cfg;
   p.hp = *hp;
-  const int err = launch_amp_finalize(a.partials, done, static_cast<zero_amp_state*>(d_state), p,
-                                      stream);
+  const int err = launch_amp_finalize(a.partials, done, static_cast<zero_amp_state*>(d_state),
+                                      bcast, p, stream);
   if (err != 0)
     return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                 cudaGetErrorString(static_cast<cudaError_t>(err)));

@@ -77,11 +77,26 @@ struct LaunchArgs {
   int64_t n_tiles;
   double* partials;                // mixed-precision: per-tile binary64 sums of squares
   int64_t tile_base;               // index of this launch's first tile among the step's
-  const zero_amp_state* amp;       // mixed-precision: device state of the controls
+  const struct AmpBcast* bcast;    // mixed-precision: copies of the decision record
   Job jobs[kMaxJobs];
 };
 
 enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kAdamwAmp };
+
+// The decision of a mixed-precision step as the update kernel needs it.  The
+// decision kernel writes kAmpCopies copies, 64 bytes apart, at the start of
+// the workspace; CTA b reads copy b % kAmpCopies with one thread, so the
+// tens of thousands of CTAs of the update do not all hit one L2 line.
+struct alignas(16) AmpBcast {
+  int32_t overflow;
+  float coef;
+  int32_t pad_[2];
+  float sc[8];
+  int32_t pad2_[4];
+};
+static_assert(sizeof(AmpBcast) == 64, "one copy per 64-byte line segment");
+constexpr int kAmpCopies = 64;
+constexpr int64_t kAmpBcastBytes = kAmpCopies * sizeof(AmpBcast);  // head of the workspace
 
 // Parameters of the one-CTA decision kernel of the mixed-precision step.
 struct AmpParams {
@@ -91,7 +106,7 @@ struct AmpParams {
 
 // Host launchers of the mixed-precision helpers (zero_launch.cu).
 int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
-                        const AmpParams& p, void* stream);
+                        AmpBcast* bcast, const AmpParams& p, void* stream);
 int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream);
 
 // Host launcher entry (zero_kernels_*.cu): launches `kind` for the jobs in

@@ -455,17 +455,23 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
 // kernel's coefficient; does nothing when the decision was to skip.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw_amp(const __grid_constant__ LaunchArgs a) {
-  if (__ldcg(&a.amp->overflow) != 0) return;
-  const float coef = __ldcg(&a.amp->coef);
+  __shared__ uint4 rec[sizeof(AmpBcast) / 16];
+  if (threadIdx.x < sizeof(AmpBcast) / 16)
+    rec[threadIdx.x] = __ldcg(reinterpret_cast<const uint4*>(a.bcast + blockIdx.x % kAmpCopies) +
+                              threadIdx.x);
+  __syncthreads();
+  const AmpBcast& d = *reinterpret_cast<const AmpBcast*>(rec);
+  if (d.overflow != 0) return;
+  const float coef = d.coef;
   StepScalars sc;
-  sc.d = __ldcg(&a.amp->sc[0]);
-  sc.b1 = __ldcg(&a.amp->sc[1]);
-  sc.b2 = __ldcg(&a.amp->sc[2]);
-  sc.c1 = __ldcg(&a.amp->sc[3]);
-  sc.c2 = __ldcg(&a.amp->sc[4]);
-  sc.ss = __ldcg(&a.amp->sc[5]);
-  sc.sb = __ldcg(&a.amp->sc[6]);
-  sc.eps = __ldcg(&a.amp->sc[7]);
+  sc.d = d.sc[0];
+  sc.b1 = d.sc[1];
+  sc.b2 = d.sc[2];
+  sc.c1 = d.sc[3];
+  sc.c2 = d.sc[4];
+  sc.ss = d.sc[5];
+  sc.sb = d.sc[6];
+  sc.eps = d.sc[7];
   for_each_tile(
       a,
       [&](const Job& jb, int64_t e0, bool two) {

@@ -43,15 +43,7 @@ int grid_for(const void* fn, int64_t n_tiles) {
 // step's coefficient and AdamW constants (binary64, each rounded once).
 constexpr int kFinalizeThreads = 1024;
 
-__global__ void __launch_bounds__(kFinalizeThreads) k_amp_finalize(const double* partials,
-                                                                   int64_t n,
-                                                                   zero_amp_state* st,
-                                                                   const AmpParams p) {
-  double s = 0.0;
-  for (int64_t i = threadIdx.x; i < n; i += kFinalizeThreads) s += __ldcg(partials + i);
-  const double sumsq = block_sum<kFinalizeThreads>(s);
-  if (threadIdx.x != 0) return;
-  zero_amp_state x = *st;
+__device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p) {
   const double S = x.scale;
   x.norm = sqrt(sumsq) / S;
   if (!isfinite(sumsq)) {
@@ -65,41 +57,74 @@ __global__ void __launch_bounds__(kFinalizeThreads) k_amp_finalize(const double*
       const double half = S / 2.0;
       x.scale = half > p.cfg.min_scale ? half : p.cfg.min_scale;
     }
-  } else {
-    double clip = 1.0;
-    if (p.cfg.max_norm > 0.0) {
-      const double q = p.cfg.max_norm / (x.norm + 1e-6);
-      if (q < 1.0) clip = q;
-    }
-    x.coef = static_cast<float>(clip / S);
-    const int64_t t = x.step + 1;
-    const zero_adamw_hparams& h = p.hp;
-    x.sc[0] = static_cast<float>(1.0 - h.lr * h.weight_decay);
-    x.sc[1] = static_cast<float>(h.beta1);
-    x.sc[2] = static_cast<float>(h.beta2);
-    x.sc[3] = static_cast<float>(1.0 - h.beta1);
-    x.sc[4] = static_cast<float>(1.0 - h.beta2);
-    x.sc[5] = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
-    x.sc[6] = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
-    x.sc[7] = static_cast<float>(h.eps);
-    x.overflow = 0;
-    x.step = t;
-    x.good_steps += 1;
-    if (p.cfg.window > 0 && x.good_steps >= p.cfg.window) {
-      x.scale = S * 2.0;
-      x.good_steps = 0;
-      x.hysteresis_left = p.cfg.hysteresis;
-    }
+    return;
   }
-  *st = x;
+  double clip = 1.0;
+  if (p.cfg.max_norm > 0.0) {
+    const double q = p.cfg.max_norm / (x.norm + 1e-6);
+    if (q < 1.0) clip = q;
+  }
+  x.coef = static_cast<float>(clip / S);
+  const int64_t t = x.step + 1;
+  const zero_adamw_hparams& h = p.hp;
+  x.sc[0] = static_cast<float>(1.0 - h.lr * h.weight_decay);
+  x.sc[1] = static_cast<float>(h.beta1);
+  x.sc[2] = static_cast<float>(h.beta2);
+  x.sc[3] = static_cast<float>(1.0 - h.beta1);
+  x.sc[4] = static_cast<float>(1.0 - h.beta2);
+  x.sc[5] = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
+  x.sc[6] = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
+  x.sc[7] = static_cast<float>(h.eps);
+  x.overflow = 0;
+  x.step = t;
+  x.good_steps += 1;
+  if (p.cfg.window > 0 && x.good_steps >= p.cfg.window) {
+    x.scale = S * 2.0;
+    x.good_steps = 0;
+    x.hysteresis_left = p.cfg.hysteresis;
+  }
+}
+
+__global__ void __launch_bounds__(kFinalizeThreads) k_amp_finalize(const double* partials,
+                                                                   int64_t n,
+                                                                   zero_amp_state* st,
+                                                                   AmpBcast* bcast,
+                                                                   const AmpParams p) {
+  // four independent running sums per thread (fixed assignment), then the
+  // block in a fixed order
+  double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+  constexpr int64_t kStride = 4 * kFinalizeThreads;
+  int64_t i = threadIdx.x;
+  for (; i + 3 * kFinalizeThreads < n; i += kStride) {
+    s0 += __ldcg(partials + i);
+    s1 += __ldcg(partials + i + kFinalizeThreads);
+    s2 += __ldcg(partials + i + 2 * kFinalizeThreads);
+    s3 += __ldcg(partials + i + 3 * kFinalizeThreads);
+  }
+  for (; i < n; i += kFinalizeThreads) s0 += __ldcg(partials + i);
+  const double sumsq = block_sum<kFinalizeThreads>((s0 + s1) + (s2 + s3));
+  __shared__ AmpBcast rec;
+  if (threadIdx.x == 0) {
+    zero_amp_state x = *st;
+    amp_decide(x, sumsq, p);
+    *st = x;
+    AmpBcast b = {};
+    b.overflow = x.overflow;
+    b.coef = x.coef;
+    for (int k = 0; k < 8; ++k) b.sc[k] = x.sc[k];
+    rec = b;
+  }
+  __syncthreads();
+  // the decision record to its kAmpCopies places, one thread each
+  if (threadIdx.x < kAmpCopies) bcast[threadIdx.x] = rec;
 }
 
 __global__ void k_amp_init(zero_amp_state* st, const zero_amp_state v) { *st = v; }
 
 int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
-                        const AmpParams& p, void* stream) {
+                        AmpBcast* bcast, const AmpParams& p, void* stream) {
   k_amp_finalize<<<1, kFinalizeThreads, 0, static_cast<cudaStream_t>(stream)>>>(partials, n_tiles,
-                                                                               state, p);
+                                                                               state, bcast, p);
   return static_cast<int>(cudaGetLastError());
 }
 
