@@ -298,6 +298,39 @@ zero_status zero_step_amp(const zero_plan* plan, const void* const* grads, zero_
                           int64_t workspace_bytes, uint64_t rank_mask, int64_t bucket_elems,
                           void* stream);
 
+/*
+ * zero_step_amp without a workspace argument, for callers that cannot
+ * allocate device memory: code whose device memory all comes from a fixed
+ * budget or pool it does not control, or that runs where a cudaMalloc /
+ * cudaFree (and the device-wide synchronisation a cudaFree can imply) is not
+ * allowed, or that has nowhere to keep a workspace alive between calls.
+ * The pages describe no such call; it is a convenience of this library.
+ *
+ * Same arguments and results as zero_step_amp, minus workspace and
+ * workspace_bytes.  The scratch is instead a fixed 1 MiB array compiled into
+ * the library, present on every GPU that loads it until the process exits;
+ * this call allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library routine).  Limits and rules:
+ *  - the step may span at most 130,560 tiles of 2048 elements, i.e.
+ *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems) <= 1 MiB (about
+ *    267 million owned elements per call); larger steps are rejected with
+ *    ZERO_ERR_INVALID and a message, and nothing is launched;
+ *  - the first call on a device looks up the array's device address with
+ *    that device current and caches it; make that first call before any
+ *    stream capture begins;
+ *  - every call on a device shares the one array, which keeps what the last
+ *    call left there (each call writes everything it reads, so nothing needs
+ *    clearing): calls whose work overlaps on the GPU (different streams,
+ *    not ordered by events) race on it and must be serialised by the caller.
+ */
+zero_status zero_step_amp_noalloc(const zero_plan* plan, const void* const* grads,
+                                  zero_dtype dtype, zero_reduce_op op, float* const* grad_shards,
+                                  float* const* master, float* const* m, float* const* v,
+                                  void* full_flat16, void* const* out16_shard,
+                                  const zero_adamw_hparams* hp, const zero_amp_config* cfg,
+                                  void* d_state, uint64_t rank_mask, int64_t bucket_elems,
+                                  void* stream);
+
 /* Synchronize `stream` and report any asynchronous device error. */
 zero_status zero_sync(void* stream);
 

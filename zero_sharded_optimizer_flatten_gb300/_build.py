@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzero.so")
 
 SOURCES = ["zero_plan.cpp", "zero_capi.cpp", "zero_launch.cu", "zero_kernels_fp16.cu",
-           "zero_kernels_bf16.cu"]
+           "zero_kernels_bf16.cu", "zero_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division and square root, no flush-to-zero, no FMA contraction of the
 # explicitly rounded arithmetic (the kernels use __f*_rn intrinsics anyway).

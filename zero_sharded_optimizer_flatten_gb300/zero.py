@@ -509,3 +509,41 @@ def zero_step_amp(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
                            _ptrs(vv), full, o16, ctypes.byref(hp), ctypes.byref(c),
                            _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
                            int(bucket_elems), _stream(stream)))
+
+
+def zero_step_amp_noalloc(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
+                          out16_shard, hparams: AdamW, cfg: AmpConfig, d_state, rank_mask=None,
+                          bucket_elems=0, stream=None, dtype=None):
+    """zero_step_amp for callers that cannot allocate device memory: the
+    scratch is the library's fixed 1 MiB device array (steps of up to
+    130,560 tiles of 2048 elements).  The first call on a device sets the
+    array up (make it before any stream capture); calls that overlap on the
+    GPU share the array and must be serialised by the caller."""
+    torch = _torch()
+    L = lib()
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    L.zero_step_amp_noalloc.argtypes = [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp,
+                                        vp, vpp, ctypes.POINTER(AdamWHparams),
+                                        ctypes.POINTER(AmpConfigC), vp, ctypes.c_uint64,
+                                        ctypes.c_int64, vp]
+    L.zero_step_amp_noalloc.restype = ctypes.c_int
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    o16 = (_ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+           if out16_shard is not None else None)
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    hp = hparams.c()
+    c = cfg.c()
+    _check(L.zero_step_amp_noalloc(plan.handle, _ptrs(g), dt, op_i, _ptrs(gs), _ptrs(ms),
+                                   _ptrs(mm), _ptrs(vv), full, o16, ctypes.byref(hp),
+                                   ctypes.byref(c), _addr(d_state, "d_state", AMP_STATE_BYTES),
+                                   mask, int(bucket_elems), _stream(stream)))
