@@ -4,10 +4,15 @@
  * One process, one GPU, N *virtual* data-parallel ranks: rank q's gradient
  * replica and rank r's optimizer shard are separate caller-owned buffers in
  * the same HBM.  The library owns only the partition plan (host memory).
- * Every tensor argument is caller-owned device memory (for example a torch
- * tensor's data_ptr()); every stream argument is a cudaStream_t passed as
- * void* (NULL = the legacy default stream).  Compute calls are asynchronous
- * on that stream.
+ * Every tensor argument is caller-owned memory the GPU can address: device
+ * memory (for example a torch tensor's data_ptr()), or host memory mapped
+ * into the GPU's address space at the same address (pinned with
+ * cudaHostAlloc / cudaHostRegister under unified addressing).  Host buffers
+ * are read and written by the kernels across the host link (NVLink-C2C on
+ * Grace-Blackwell), which replaces an explicit copy; they run at the link's
+ * bandwidth instead of HBM's.  Every stream argument is a cudaStream_t passed
+ * as void* (NULL = the legacy default stream).  Compute calls are
+ * asynchronous on that stream.
  *
  * Sources (page title, section) for what each call computes:
  *  [ZeRO-2 blog]   "DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com):

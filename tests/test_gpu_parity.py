@@ -308,3 +308,25 @@ def test_llama13b_zero3_layer_pass_sampled():
         torch.cuda.synchronize()
         assert torch.equal(layer_buf, torch.cat(shards))
         del g, shards, master, m, v, p16
+
+
+@pytest.mark.parametrize("mode,N,dtype", [("flat", 8, "bf16"), ("round_robin", 4, "fp16")])
+def test_host_buffers_through_the_link(mode, N, dtype):
+    """Gradient replicas in pinned host memory and the gathered parameters
+    written to pinned host memory: bit-identical to device buffers."""
+    w = W.small((30000, 37, 4096, 3, 129), N, mode=mode, align=16, dtype=dtype, op="avg")
+    dev_case = Case(w, with_oracle=False)
+    host_case = Case(w, with_oracle=False)
+    host_full = torch.zeros(host_case.L, dtype=w.torch_dtype, pin_memory=True)
+    for t in (1, 2):
+        g = dev_case.grads(t)
+        hg = [x.cpu().pin_memory() for x in g]
+        Z.zero_step(dev_case.plan, g, "avg", dev_case.master, dev_case.m, dev_case.v,
+                    dev_case.full16, None, HP, t)
+        Z.zero_step(host_case.plan, hg, "avg", host_case.master, host_case.m, host_case.v,
+                    host_full, None, HP, t)
+        torch.cuda.synchronize()
+    for r in range(N):
+        assert torch.equal(dev_case.master[r], host_case.master[r])
+        assert torch.equal(dev_case.v[r], host_case.v[r])
+    assert torch.equal(dev_case.full16.cpu(), host_full)

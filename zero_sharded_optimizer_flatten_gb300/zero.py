@@ -1,7 +1,8 @@
 """Python binding of the C ABI in include/zero.h (ctypes; argument marshalling only).
 
 Every function keeps the C name and forwards to libzero.so.  Tensors are
-torch tensors on the GPU (or raw integer device addresses); the binding only
+torch tensors on the GPU or in pinned host memory (which the kernels read and
+write across the host link), or raw integer addresses; the binding only
 checks dtypes, devices, contiguity and sizes against the plan, turns them into
 pointer arrays and passes the current CUDA stream.  There is no fallback: if
 libzero.so is missing the first call raises.
@@ -233,8 +234,8 @@ def _addr(t, what: str, min_numel: Optional[int] = None, dtype=None) -> int:
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{what}: expected a torch.Tensor or an int address")
-    if not t.is_cuda:
-        raise ValueError(f"{what}: tensor must be on a CUDA device")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{what}: tensor must be on a CUDA device or in pinned host memory")
     if not t.is_contiguous():
         raise ValueError(f"{what}: tensor must be contiguous")
     if dtype is not None and t.dtype != dtype:
