@@ -288,7 +288,7 @@ class FlatRunner:
     (bucketed if the workload says so).  Gradient buffers hold only the flat
     range the masked ranks own."""
 
-    def __init__(self, w, dev, grad_sets, amp=None):
+    def __init__(self, w, dev, grad_sets, amp=None, offload=False):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
@@ -301,9 +301,17 @@ class FlatRunner:
         p16 = W.fill(w, "param", 0, 0, 0, ext, torch.empty(ext, dtype=w.torch_dtype, device=dev))
         self.full16 = torch.zeros_like(p16)
         S = [plan.shard_len(r) if (self.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
-        self.master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
-        self.m = [torch.empty_like(x) for x in self.master]
-        self.v = [torch.empty_like(x) for x in self.master]
+        # offload: the fp32 optimizer state lives in pinned host memory and the
+        # kernels stream it across the host link
+        self.offload = offload
+
+        def state(n):
+            if offload:
+                return torch.empty(n, dtype=torch.float32, pin_memory=True)
+            return torch.empty(n, dtype=torch.float32, device=dev)
+        self.master = [state(n) for n in S]
+        self.m = [state(n) for n in S]
+        self.v = [state(n) for n in S]
         Z.zero_init_shards(plan, p16, self.master, self.m, self.v, rank_mask=self.mask)
         del p16
         self.grads = [[W.grads16(w, s + 1, q, dev, 0, ext) for q in range(w.n_ranks)]
@@ -455,7 +463,7 @@ def run_gpu(args, world, rank, local):
         if args.amp:
             amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
                               max_norm=args.max_norm)
-        run = FlatRunner(w, dev, args.grad_sets, amp)
+        run = FlatRunner(w, dev, args.grad_sets, amp, args.offload)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -501,7 +509,7 @@ def run_gpu(args, world, rank, local):
         bytes_per_launch = run.bytes_per_step
 
     e2e = None
-    if not w.zero3 and not args.amp:
+    if not w.zero3 and not args.amp and not args.offload:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         per_step, h2d, d2h = run.e2e(t, e2e_steps)
         best = min(per_step, key=per_step.get)
@@ -556,6 +564,14 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks.summary(wall0, wall1),
     }
+    if args.offload:
+        link = 24 * run.elems
+        line["config"]["offload"] = {
+            "state": "fp32 master/m/v in pinned host memory, streamed by the kernels",
+            "host_link_bytes_per_step": link,
+            "host_link_gbs": link / (elapsed / args.steps) / 1e9,
+            "hbm_bytes_per_step": run.bytes_per_step - link,
+        }
     if args.amp:
         line["config"]["amp"] = {"max_norm": args.max_norm, "init_scale": 1.0,
                                  "note": "loss-scale check, global-norm clipping, skip on overflow"}
@@ -590,6 +606,9 @@ def main(argv=None):
     ap.add_argument("--amp", action="store_true",
                     help="time the mixed-precision step (norm check + clipping) instead")
     ap.add_argument("--max-norm", type=float, default=1.0)
+    ap.add_argument("--offload", action="store_true",
+                    help="keep the fp32 optimizer state in pinned host memory (ZeRO-Offload "
+                         "over the host link)")
     ap.add_argument("--layer-states", type=int, default=40,
                     help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")
     args = ap.parse_args(argv)

@@ -330,3 +330,28 @@ def test_host_buffers_through_the_link(mode, N, dtype):
         assert torch.equal(dev_case.master[r], host_case.master[r])
         assert torch.equal(dev_case.v[r], host_case.v[r])
     assert torch.equal(dev_case.full16.cpu(), host_full)
+
+
+def test_optimizer_state_in_host_memory():
+    """ZeRO-Offload over the host link: fp32 master/m/v in pinned host memory,
+    gradients and parameters in HBM; bit-identical to device-resident state,
+    through init, the fused step and the unfused pieces."""
+    w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    dev_case = Case(w, with_oracle=False)
+    plan = dev_case.plan
+    S = [plan.shard_len(r) for r in range(4)]
+    hm = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in S]
+    hmm = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in S]
+    hv = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in S]
+    full = torch.zeros_like(dev_case.full16)
+    Z.zero_init_shards(plan, dev_case.p16, hm, hmm, hv)
+    for t in (1, 2):
+        g = dev_case.grads(t)
+        Z.zero_step(plan, g, "avg", dev_case.master, dev_case.m, dev_case.v, dev_case.full16, None,
+                    HP, t)
+        Z.zero_step(plan, g, "avg", hm, hmm, hv, full, None, HP, t)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(dev_case.master[r].cpu(), hm[r])
+        assert torch.equal(dev_case.m[r].cpu(), hmm[r]) and torch.equal(dev_case.v[r].cpu(), hv[r])
+    assert torch.equal(dev_case.full16, full)
