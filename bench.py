@@ -403,7 +403,7 @@ class Zero3Runner:
     shard (the next gather's source).  One gradient set is shared by all
     layers (the backward pass refills one buffer per layer)."""
 
-    def __init__(self, w, dev, layer_states):
+    def __init__(self, w, dev, layer_states, prefetch=0):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
@@ -416,7 +416,7 @@ class Zero3Runner:
         self.layer_buf = torch.empty(L, dtype=w.torch_dtype, device=dev)
         self.grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
         self.n_states = min(w.layers, layer_states)
-        self.shards, self.calls = [], []
+        self.shards, self.calls, self.states = [], [], []
         for layer in range(self.n_states):
             p16 = W.params16(w, dev, layer=layer)
             sh = [p16[sum(S[:r]):sum(S[:r]) + S[r]].clone() for r in range(w.n_ranks)]
@@ -426,14 +426,35 @@ class Zero3Runner:
             Z.zero_init_shards(plan, p16, master, m, v)
             del p16
             self.shards.append(sh)
+            self.states.append((master, m, v))
             self.calls.append(Z.ZeroStep(plan, self.grads, w.op, master, m, v, None, sh, self.hp))
         self.layers = w.layers
+        self.prefetch = prefetch
+        if prefetch:
+            if w.layers % self.n_states:
+                raise SystemExit("--prefetch needs the layer count to be a multiple of "
+                                 "--layer-states")
+            layers = [{"grads": self.grads, "master": st[0], "m": st[1], "v": st[2],
+                       "shards16": self.shards[k]} for k, st in enumerate(self.states)]
+            bufs = [self.layer_buf] + [torch.empty_like(self.layer_buf)
+                                       for _ in range(prefetch - 1)]
+            self.passes = Z.Zero3Pass(plan, layers, bufs, w.op, self.hp)
+            self.gather_stream = torch.cuda.Stream(dev)
         self.elems = w.layers * plan.padded
         self.bytes_per_step = w.layers * (step_bytes(plan.padded, w.n_ranks) + 4 * plan.padded)
         self.kernel_bytes = step_bytes(plan.padded, w.n_ranks)  # per k_step launch
         self.kernel = KERNEL_PREFIX
 
     def step(self, t, events=None):
+        if self.prefetch:
+            # the native layer stream: gathers on their own stream run ahead
+            if events is not None:
+                events[0][0].record()
+            for k in range(self.layers // self.n_states):
+                self.passes(t, gather_stream=self.gather_stream)
+            if events is not None:
+                events[0][1].record()
+            return
         for layer in range(self.layers):
             k = layer % self.n_states
             self.Z.zero_allgather(self.plan, self.shards[k], self.layer_buf)
@@ -457,7 +478,7 @@ def run_gpu(args, world, rank, local):
     w = W.WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
     if w.zero3:
-        run = Zero3Runner(w, dev, args.layer_states)
+        run = Zero3Runner(w, dev, args.layer_states, args.prefetch)
     else:
         amp = None
         if args.amp:
@@ -480,7 +501,8 @@ def run_gpu(args, world, rank, local):
     def pair():
         return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     if w.zero3:
-        ev = [[pair() for _ in range(run.layers)] for _ in range(args.steps)]
+        ev = [[pair() for _ in range(1 if run.prefetch else run.layers)]
+              for _ in range(args.steps)]
     else:
         ev = [pair() for _ in range(args.steps)]
     barrier(dist, local)
@@ -501,7 +523,11 @@ def run_gpu(args, world, rank, local):
     clocks.stop()
     elapsed = start.elapsed_time(stop) / 1e3
     elapsed = max_over_ranks(dist, elapsed, local)
-    if w.zero3:
+    if w.zero3 and run.prefetch:
+        # events bracket whole passes: report the pass's bytes (gathers + steps)
+        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
+        bytes_per_launch = run.bytes_per_step
+    elif w.zero3:
         kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
         bytes_per_launch = run.kernel_bytes
     else:
@@ -582,6 +608,9 @@ def run_gpu(args, world, rank, local):
         line["config"]["amp"] = {"max_norm": args.max_norm, "init_scale": 1.0,
                                  "note": "loss-scale check, global-norm clipping, skip on overflow"}
     if w.zero3:
+        if run.prefetch:
+            line["roofline"]["kernel"] = "zero_zero3_pass (k_allgather + k_step per layer)"
+            line["config"]["prefetch_layer_buffers"] = run.prefetch
         line["config"]["layer_states"] = run.n_states
         line["config"]["layers"] = run.layers
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -615,6 +644,9 @@ def main(argv=None):
     ap.add_argument("--offload", action="store_true",
                     help="keep the fp32 optimizer state in pinned host memory (ZeRO-Offload "
                          "over the host link)")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="ZeRO-3 stream through zero_zero3_pass with this many layer buffers "
+                         "(gathers on a second stream); 0 = serial Python loop")
     ap.add_argument("--layer-states", type=int, default=40,
                     help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")
     args = ap.parse_args(argv)

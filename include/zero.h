@@ -226,6 +226,45 @@ zero_status zero_step(const zero_plan* plan, const void* const* grads, zero_dtyp
                       int64_t step, uint64_t rank_mask, int64_t bucket_elems, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* ZeRO-3 layer stream with prefetch                                        */
+/* ------------------------------------------------------------------------ */
+/*
+ * ZeRO-3 keeps only 16-bit shards of every layer and gathers a layer's full
+ * parameters just before it is used, releasing them afterwards ("ZeRO 优化器"
+ * (cookllm.com), ZeRO Stage 3: per-layer gather -> compute -> release;
+ * "ZeRO / DeepSpeed 深度解读报告" §2.4; "DeepSpeed ZeRO-2 ..." §5 names the
+ * prefetch bucket).  One layer of a stack that shares one plan: */
+typedef struct {
+  const void* const* grads; /* n_ranks 16-bit flat gradient replicas of the layer   */
+  float* const* master;     /* n_ranks fp32 shards (read-modify-write)               */
+  float* const* m;          /* n_ranks fp32 shards (read-modify-write)               */
+  float* const* v;          /* n_ranks fp32 shards (read-modify-write)               */
+  void* const* shards16;    /* n_ranks 16-bit shards: gather source, step output     */
+} zero_layer;
+
+/*
+ * One pass over n_layers layers: for layer l, zero_allgather(shards16 ->
+ * layer_bufs[l % n_bufs]) on gather_stream, then zero_step(grads, master, m,
+ * v, full_flat16 = NULL, out16_shard = shards16) on step_stream for step
+ * `step`.  Ordering, enforced with events (no host waits):
+ *   - the gather of layer l starts after the step of layer l - n_bufs
+ *     finished (the layer buffer it overwrites is released then);
+ *   - the step of layer l starts after the gather of layer l (the step
+ *     rewrites the shards the gather reads);
+ *   - the first gather starts after all work already queued on step_stream.
+ * So with two streams and n_bufs >= 2 the gathers of the next layers run
+ * ahead (prefetch) while earlier layers update; with gather_stream ==
+ * step_stream the pass is serial.  All work of the pass is complete once
+ * step_stream reaches the point after the call.  Results do not depend on
+ * n_bufs or the streams.  n_bufs in [1, 64]; every layer buffer holds
+ * `padded` 16-bit elements.
+ */
+zero_status zero_zero3_pass(const zero_plan* plan, const zero_layer* layers, int32_t n_layers,
+                            void* const* layer_bufs, int32_t n_bufs, zero_dtype dtype,
+                            zero_reduce_op op, const zero_adamw_hparams* hp, int64_t step,
+                            void* gather_stream, void* step_stream);
+
+/* ------------------------------------------------------------------------ */
 /* Mixed-precision controls: dynamic loss scaling, overflow skip, clipping  */
 /* ------------------------------------------------------------------------ */
 /*

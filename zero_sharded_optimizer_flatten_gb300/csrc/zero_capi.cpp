@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <inttypes.h>
 #include <math.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -467,6 +468,106 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
                 cudaGetErrorString(static_cast<cudaError_t>(err)));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return run_buckets(fn, Kind::kAdamwAmp, dtype, plan, rank_mask, 0, a, stream);
+}
+
+namespace {
+
+// Events reused by zero_zero3_pass on this thread (created on first use,
+// timing disabled; never destroyed before the thread exits).
+struct EventPool {
+  std::vector<cudaEvent_t> ev;
+  ~EventPool() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+};
+
+zero_status pool_events(const char* fn, size_t n, std::vector<cudaEvent_t>** out) {
+  static thread_local EventPool pool;
+  while (pool.ev.size() < n) {
+    cudaEvent_t e;
+    const cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (err != cudaSuccess)
+      return fail(ZERO_ERR_CUDA, "%s: cudaEventCreateWithFlags: %s", fn, cudaGetErrorString(err));
+    pool.ev.push_back(e);
+  }
+  *out = &pool.ev;
+  return ZERO_OK;
+}
+
+zero_status cuda_ok(const char* fn, const char* what, cudaError_t e) {
+  if (e != cudaSuccess) return fail(ZERO_ERR_CUDA, "%s: %s: %s", fn, what, cudaGetErrorString(e));
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" zero_status zero_zero3_pass(const zero_plan* plan, const zero_layer* layers,
+                                       int32_t n_layers, void* const* layer_bufs, int32_t n_bufs,
+                                       zero_dtype dtype, zero_reduce_op op,
+                                       const zero_adamw_hparams* hp, int64_t step,
+                                       void* gather_stream, void* step_stream) {
+  const char* fn = "zero_zero3_pass";
+  clear_error();
+  if (!plan) return fail(ZERO_ERR_INVALID, "%s: plan is NULL", fn);
+  const uint64_t all = plan->n_ranks >= 64 ? ~UINT64_C(0) : ((UINT64_C(1) << plan->n_ranks) - 1);
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, step));
+  if (!layers || n_layers < 1) return fail(ZERO_ERR_INVALID, "%s: need n_layers >= 1 layers", fn);
+  if (!layer_bufs || n_bufs < 1 || n_bufs > 64)
+    return fail(ZERO_ERR_INVALID, "%s: need 1 <= n_bufs <= 64 layer buffers", fn);
+  for (int32_t b = 0; b < n_bufs; ++b) {
+    if (!layer_bufs[b]) return fail(ZERO_ERR_INVALID, "%s: layer_bufs[%d] is NULL", fn, b);
+    if (!aligned16(layer_bufs[b])) return fail(ZERO_ERR_ALIGN, "%s: layer_bufs[%d] is not 16-byte aligned", fn, b);
+  }
+  // every layer's pointers are checked before anything is launched
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const zero_layer& L = layers[l];
+    char msg[1024];
+    const zero_status st0 = check_ptrs(fn, "grads", L.grads, plan, all, false, true);
+    if (st0 != ZERO_OK) {
+      snprintf(msg, sizeof msg, "%s", error_buffer());
+      return fail(st0, "%s (layer %d)", msg, l);
+    }
+    const void* const* per[4] = {reinterpret_cast<const void* const*>(L.master),
+                                 reinterpret_cast<const void* const*>(L.m),
+                                 reinterpret_cast<const void* const*>(L.v),
+                                 reinterpret_cast<const void* const*>(L.shards16)};
+    const char* names[4] = {"master", "m", "v", "shards16"};
+    for (int k = 0; k < 4; ++k) {
+      const zero_status st = check_ptrs(fn, names[k], per[k], plan, all, false);
+      if (st != ZERO_OK) {
+        snprintf(msg, sizeof msg, "%s", error_buffer());
+        return fail(st, "%s (layer %d)", msg, l);
+      }
+    }
+  }
+  ZERO_TRY(pending_error(fn));
+  std::vector<cudaEvent_t>* ev = nullptr;
+  ZERO_TRY(pool_events(fn, static_cast<size_t>(n_bufs) + 2, &ev));
+  cudaEvent_t entry = (*ev)[0], gathered = (*ev)[1];
+  cudaStream_t gs = static_cast<cudaStream_t>(gather_stream);
+  cudaStream_t ss = static_cast<cudaStream_t>(step_stream);
+  const bool two = gs != ss;
+  if (two) {
+    ZERO_TRY(cuda_ok(fn, "cudaEventRecord", cudaEventRecord(entry, ss)));
+    ZERO_TRY(cuda_ok(fn, "cudaStreamWaitEvent", cudaStreamWaitEvent(gs, entry, 0)));
+  }
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const zero_layer& L = layers[l];
+    cudaEvent_t released = (*ev)[2 + l % n_bufs];
+    if (two && l >= n_bufs)
+      ZERO_TRY(cuda_ok(fn, "cudaStreamWaitEvent", cudaStreamWaitEvent(gs, released, 0)));
+    ZERO_TRY(zero_allgather(plan, L.shards16, dtype, layer_bufs[l % n_bufs], all, gather_stream));
+    if (two) {
+      ZERO_TRY(cuda_ok(fn, "cudaEventRecord", cudaEventRecord(gathered, gs)));
+      ZERO_TRY(cuda_ok(fn, "cudaStreamWaitEvent", cudaStreamWaitEvent(ss, gathered, 0)));
+    }
+    ZERO_TRY(zero_step(plan, L.grads, dtype, op, L.master, L.m, L.v, nullptr, L.shards16, hp,
+                       step, all, 0, step_stream));
+    if (two) ZERO_TRY(cuda_ok(fn, "cudaEventRecord", cudaEventRecord(released, ss)));
+  }
+  return ZERO_OK;
 }
 
 extern "C" zero_status zero_sync(void* stream) {

@@ -548,3 +548,72 @@ def zero_step_amp_noalloc(plan: Plan, grads, op, grad_shards, master, m, v, full
                                    _ptrs(mm), _ptrs(vv), full, o16, ctypes.byref(hp),
                                    ctypes.byref(c), _addr(d_state, "d_state", AMP_STATE_BYTES),
                                    mask, int(bucket_elems), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# ZeRO-3 layer stream
+
+
+class _LayerC(ctypes.Structure):
+    _fields_ = [("grads", ctypes.POINTER(ctypes.c_void_p)),
+                ("master", ctypes.POINTER(ctypes.c_void_p)),
+                ("m", ctypes.POINTER(ctypes.c_void_p)),
+                ("v", ctypes.POINTER(ctypes.c_void_p)),
+                ("shards16", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class Zero3Pass:
+    """A prepared ZeRO-3 pass over a stack of layers sharing one plan.
+
+    layers: sequence of dicts with keys grads, master, m, v, shards16 (each a
+    list of n_ranks tensors); layer_bufs: the 16-bit layer buffers the gathers
+    write, used round-robin (two or more let gathers run ahead)."""
+
+    def __init__(self, plan: Plan, layers, layer_bufs, op, hparams: AdamW, dtype=None):
+        torch = _torch()
+        all_mask = plan.all_ranks
+        self.plan = plan
+        self._arrays = []
+        self._layers = (_LayerC * len(layers))()
+        dt = None
+        for i, L in enumerate(layers):
+            if len(L["grads"]) != plan.n_ranks:
+                raise ValueError(f"layer {i}: expected {plan.n_ranks} gradient replicas")
+            g = _ptrs([_addr(t, f"layer {i} grads[{q}]", plan.padded)
+                       for q, t in enumerate(L["grads"])])
+            parts = [g]
+            for key in ("master", "m", "v"):
+                parts.append(_ptrs(_per_rank(plan, L[key], f"layer {i} {key}", all_mask,
+                                             torch.float32)))
+            parts.append(_ptrs(_per_rank(plan, L["shards16"], f"layer {i} shards16", all_mask)))
+            self._arrays.append(parts)
+            vpp = ctypes.POINTER(ctypes.c_void_p)
+            self._layers[i] = _LayerC(*[ctypes.cast(a, vpp) for a in parts])
+            if dt is None:
+                dt = _sixteen(L["grads"]) if dtype is None else dtype
+        self.dt = dt
+        self._bufs = _ptrs([_addr(b, f"layer_bufs[{k}]", plan.padded)
+                            for k, b in enumerate(layer_bufs)])
+        self.n_layers, self.n_bufs = len(layers), len(layer_bufs)
+        self.op = _OPS[op] if isinstance(op, str) else int(op)
+        self._hp = hparams.c()
+        self._keep = (layers, layer_bufs)
+        L_ = lib()
+        L_.zero_zero3_pass.argtypes = [ctypes.c_void_p, ctypes.POINTER(_LayerC), ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                       ctypes.c_int, ctypes.c_int, ctypes.POINTER(AdamWHparams),
+                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        L_.zero_zero3_pass.restype = ctypes.c_int
+
+    def __call__(self, step: int, gather_stream=None, step_stream=None):
+        ss = _stream(step_stream)
+        gs = _stream(gather_stream) if gather_stream is not None else ss
+        _check(lib().zero_zero3_pass(self.plan.handle, self._layers, self.n_layers, self._bufs,
+                                     self.n_bufs, self.dt, self.op, ctypes.byref(self._hp),
+                                     int(step), gs, ss))
+
+
+def zero_zero3_pass(plan: Plan, layers, layer_bufs, op, hparams: AdamW, step: int,
+                    gather_stream=None, step_stream=None, dtype=None):
+    """One ZeRO-3 pass (see include/zero.h); one-shot form of Zero3Pass."""
+    Zero3Pass(plan, layers, layer_bufs, op, hparams, dtype)(step, gather_stream, step_stream)
