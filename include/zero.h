@@ -185,6 +185,20 @@ zero_status zero_reduce_scatter(const zero_plan* plan, const void* const* grads,
                                 uint64_t rank_mask, int64_t bucket_elems, void* stream);
 
 /*
+ * zero_reduce_scatter restricted to the flat index range [flat_lo, flat_hi)
+ * (0 <= flat_lo <= flat_hi <= padded): one gradient bucket.  This is the call
+ * a backward pass makes as soon as every rank's replica holds a bucket's
+ * gradients ("DeepSpeed ZeRO-2 ..." §2.2, §4.2: IPG buckets of
+ * reduce_bucket_size reduced on a side stream while the backward pass goes
+ * on, overlap_comm).  Only grad_shards elements whose flat index falls in the
+ * range are written; an empty intersection launches nothing.
+ */
+zero_status zero_reduce_scatter_range(const zero_plan* plan, const void* const* grads,
+                                      zero_dtype dtype, zero_reduce_op op,
+                                      float* const* grad_shards, uint64_t rank_mask,
+                                      int64_t flat_lo, int64_t flat_hi, void* stream);
+
+/*
  * Local AdamW step on each masked rank's shard ([ZeRO-2 blog] §4.3), one
  * binary32 rounding per operation, in this order (t = step >= 1):
  *   p = p*d;  m = b1*m + c1*g;  v = b2*v + c2*(g*g);

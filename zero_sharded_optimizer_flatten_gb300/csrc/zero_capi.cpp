@@ -285,6 +285,35 @@ extern "C" zero_status zero_reduce_scatter(const zero_plan* plan, const void* co
   return run_buckets(fn, Kind::kReduceScatter, dtype, plan, rank_mask, bucket_elems, a, stream);
 }
 
+extern "C" zero_status zero_reduce_scatter_range(const zero_plan* plan, const void* const* grads,
+                                                 zero_dtype dtype, zero_reduce_op op,
+                                                 float* const* grad_shards, uint64_t rank_mask,
+                                                 int64_t flat_lo, int64_t flat_hi, void* stream) {
+  const char* fn = "zero_reduce_scatter_range";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  if (flat_lo < 0 || flat_hi < flat_lo || flat_hi > plan->padded)
+    return fail(ZERO_ERR_INVALID, "%s: range [%" PRId64 ", %" PRId64 ") outside [0, %" PRId64 "]", fn,
+                flat_lo, flat_hi, plan->padded);
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (in_mask(rank_mask, r)) a.gshard[r] = grad_shards[r];
+  }
+  set_scale(a, plan->n_ranks, op);
+  std::vector<Job> jobs;
+  build_jobs(plan, rank_mask, flat_lo, flat_hi, jobs);
+  if (jobs.empty()) return ZERO_OK;
+  return launch_jobs(fn, Kind::kReduceScatter, dtype, a, jobs, stream, nullptr);
+}
+
 extern "C" zero_status zero_adamw_shard_step(const zero_plan* plan, float* const* master,
                                              float* const* m, float* const* v,
                                              const float* const* grad_shards,

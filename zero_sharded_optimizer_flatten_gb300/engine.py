@@ -1,0 +1,163 @@
+"""A ZeRO data-parallel engine over N virtual ranks on one GPU.
+
+It wires a model's backward pass into the library's calls the way
+"DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com) §2.1 and §4.1-§4.4
+describe the optimizer doing it:
+
+* the parameters are flattened into one 16-bit buffer (and become views of
+  it), which the plan partitions across the ranks;
+* every virtual rank q owns one flat gradient replica (contiguous gradients);
+  a post-accumulate-grad hook copies each parameter's gradient into rank q's
+  replica and releases ``param.grad`` (the ZeRO-2 release of gradients);
+* the replicas are cut into buckets of ``bucket_elems`` flat elements (the
+  IPG bucket, reduce_bucket_size); as soon as every rank has filled a bucket,
+  its reduce-scatter is launched -- on a side stream when ``overlap_comm`` so
+  it runs while the backward pass goes on;
+* ``step()`` waits for the reductions, runs AdamW on every rank's fp32 shard,
+  casts to 16 bits and all-gathers into the flat buffer, so the model's
+  parameters hold the new values.
+
+The arithmetic is the library's (no compute happens here); this module only
+does bookkeeping and launches.
+"""
+from __future__ import annotations
+
+from typing import Iterable, List, Optional
+
+import torch
+
+from . import zero as Z
+
+
+class ZeroEngine:
+    def __init__(self, params: Iterable[torch.nn.Parameter], n_ranks: int, *, mode="flat",
+                 align: int = 16, op: str = "avg", hparams: Optional[Z.AdamW] = None,
+                 bucket_elems: int = 50_000_000, overlap_comm: bool = True):
+        self.params: List[torch.nn.Parameter] = list(params)
+        if not self.params:
+            raise ValueError("no parameters")
+        dt = self.params[0].dtype
+        dev = self.params[0].device
+        if dt not in (torch.float16, torch.bfloat16):
+            raise TypeError("parameters must be float16 or bfloat16 (the 16-bit model copy)")
+        for p in self.params:
+            if p.dtype != dt or p.device != dev or not p.is_cuda:
+                raise ValueError("all parameters must share one 16-bit dtype and one CUDA device")
+        self.n_ranks, self.op = n_ranks, op
+        self.hp = hparams or Z.AdamW()
+        self.numel = [p.numel() for p in self.params]
+        self.plan = plan = Z.zero_plan_partitions(self.numel, n_ranks, mode, align)
+        P, phi = plan.padded, plan.phi
+        # flat 16-bit parameters; the model's parameters become views of it
+        self.flat16 = torch.zeros(P, dtype=dt, device=dev)
+        self.offsets, off = [], 0
+        with torch.no_grad():
+            for p, n in zip(self.params, self.numel):
+                self.flat16[off:off + n].copy_(p.reshape(-1))
+                p.data = self.flat16[off:off + n].view_as(p)
+                self.offsets.append(off)
+                off += n
+        # per-rank gradient replicas, fp32 gradient shards, optimizer state
+        self.grads = [torch.zeros(P, dtype=dt, device=dev) for _ in range(n_ranks)]
+        S = [plan.shard_len(r) for r in range(n_ranks)]
+        self.grad_shards = [torch.zeros(n, dtype=torch.float32, device=dev) for n in S]
+        self.master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+        self.m = [torch.empty_like(x) for x in self.master]
+        self.v = [torch.empty_like(x) for x in self.master]
+        self.shard16 = [torch.empty(n, dtype=dt, device=dev) for n in S]
+        Z.zero_init_shards(plan, self.flat16, self.master, self.m, self.v)
+        # buckets over the flat index space; the tail padding needs no filling
+        B = bucket_elems if bucket_elems > 0 else P
+        self.buckets = [(lo, min(lo + B, P)) for lo in range(0, P, B)]
+        self._need = [max(0, min(hi, phi) - min(lo, phi)) for lo, hi in self.buckets]
+        self._tensor_buckets = []
+        for k, (o, n) in enumerate(zip(self.offsets, self.numel)):
+            parts = []
+            for b in range(o // B, (o + n - 1) // B + 1 if n else o // B):
+                lo, hi = self.buckets[b]
+                cnt = min(hi, o + n) - max(lo, o)
+                if cnt > 0:
+                    parts.append((b, cnt))
+            self._tensor_buckets.append(parts)
+        self.reduction_stream = torch.cuda.Stream(dev) if overlap_comm else None
+        self.step_count = 0
+        self.launched_during_backward = 0
+        self._current: Optional[int] = None
+        self._reset()
+        self._hooks = [p.register_post_accumulate_grad_hook(self._hook(k))
+                       for k, p in enumerate(self.params)]
+
+    # ------------------------------------------------------------------
+    def _reset(self):
+        nb = len(self.buckets)
+        self._filled = [[0] * nb for _ in range(self.n_ranks)]
+        self._ranks_done = [0] * nb
+        self._launched = [False] * nb
+        self._seen = [False] * self.n_ranks
+
+    def _hook(self, k: int):
+        def hook(p: torch.nn.Parameter):
+            q = self._current
+            if q is None or p.grad is None:
+                return  # a backward pass outside backward(): leave .grad alone
+            o, n = self.offsets[k], self.numel[k]
+            self.grads[q][o:o + n].copy_(p.grad.reshape(-1))
+            p.grad = None
+            for b, cnt in self._tensor_buckets[k]:
+                self._filled[q][b] += cnt
+                if self._filled[q][b] == self._need[b]:
+                    self._ranks_done[b] += 1
+                    if self._ranks_done[b] == self.n_ranks:
+                        self._launch(b)
+                        self.launched_during_backward += 1
+        return hook
+
+    def _launch(self, b: int):
+        lo, hi = self.buckets[b]
+        if self.reduction_stream is None:
+            Z.zero_reduce_scatter_range(self.plan, self.grads, self.op, self.grad_shards, lo, hi)
+        else:
+            # the replica copies were queued on the current stream
+            self.reduction_stream.wait_stream(torch.cuda.current_stream())
+            Z.zero_reduce_scatter_range(self.plan, self.grads, self.op, self.grad_shards, lo, hi,
+                                        stream=self.reduction_stream)
+        self._launched[b] = True
+
+    # ------------------------------------------------------------------
+    def backward(self, loss: torch.Tensor, rank: int):
+        """loss.backward() for virtual rank `rank` (its micro-batch)."""
+        if not 0 <= rank < self.n_ranks:
+            raise ValueError(f"rank {rank} out of range")
+        if self._seen[rank]:
+            raise RuntimeError(f"rank {rank} already ran backward in this iteration")
+        self._current = rank
+        try:
+            loss.backward()
+        finally:
+            self._current = None
+        self._seen[rank] = True
+        for b, need in enumerate(self._need):
+            if need == 0 and not self._launched[b] and all(self._seen):
+                self._launch(b)  # buckets of padding only
+
+    def step(self):
+        """Wait for the reductions, then AdamW + cast + all-gather."""
+        if not all(self._seen):
+            missing = [q for q in range(self.n_ranks) if not self._seen[q]]
+            raise RuntimeError(f"ranks {missing} did not run backward in this iteration")
+        for b, done in enumerate(self._launched):
+            if not done:
+                raise RuntimeError(f"bucket {b} was not filled by every rank (a parameter "
+                                   "received no gradient?)")
+        if self.reduction_stream is not None:
+            torch.cuda.current_stream().wait_stream(self.reduction_stream)
+        self.step_count += 1
+        Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
+                                self.shard16, self.hp, self.step_count)
+        Z.zero_allgather(self.plan, self.shard16, self.flat16)
+        self._reset()
+
+    def remove_hooks(self):
+        for h in self._hooks:
+            h.remove()
+        self._hooks = []

@@ -617,3 +617,23 @@ def zero_zero3_pass(plan: Plan, layers, layer_bufs, op, hparams: AdamW, step: in
                     gather_stream=None, step_stream=None, dtype=None):
     """One ZeRO-3 pass (see include/zero.h); one-shot form of Zero3Pass."""
     Zero3Pass(plan, layers, layer_bufs, op, hparams, dtype)(step, gather_stream, step_stream)
+
+
+def zero_reduce_scatter_range(plan: Plan, grads, op, grad_shards, flat_lo: int, flat_hi: int,
+                              rank_mask=None, stream=None, dtype=None):
+    """Reduce-scatter of the flat range [flat_lo, flat_hi) only (one bucket)."""
+    torch = _torch()
+    L = lib()
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    L.zero_reduce_scatter_range.argtypes = [vp, vpp, ctypes.c_int, ctypes.c_int, vpp,
+                                            ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, vp]
+    L.zero_reduce_scatter_range.restype = ctypes.c_int
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", plan.flat_extent(mask)) for q, t in enumerate(grads)]
+    out = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    _check(L.zero_reduce_scatter_range(plan.handle, _ptrs(g), dt, op_i, _ptrs(out), mask,
+                                       int(flat_lo), int(flat_hi), _stream(stream)))
