@@ -622,6 +622,65 @@ def run_gpu(args, world, rank, local):
     return 0
 
 
+def run_engine(args, world, rank, local):
+    """A training iteration of the ToyModel group (hidden 1024, 12 layers,
+    round-robin over 4 virtual ranks) through the autograd-driven engine:
+    4 x (forward + backward on the rank's micro-batch) + step, timed with and
+    without overlapping the bucket reduce-scatters with the backward pass."""
+    import torch
+
+    from zero_sharded_optimizer_flatten_gb300.engine import ZeroEngine
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def toy():
+        torch.manual_seed(0)
+        layers = []
+        for _ in range(12):
+            layers += [torch.nn.Linear(1024, 4096), torch.nn.GELU(), torch.nn.Linear(4096, 1024)]
+        layers.append(torch.nn.Linear(1024, 10))
+        return torch.nn.Sequential(*layers).to(dev, torch.bfloat16)
+
+    N = 4
+    xs = [torch.randn(args.tokens, 1024, device=dev, dtype=torch.bfloat16) for _ in range(N)]
+    out = {}
+    for overlap in (False, True):
+        model = toy()
+        eng = ZeroEngine(model.parameters(), N, mode="round_robin", op="sum",
+                         bucket_elems=args.bucket, overlap_comm=overlap)
+
+        def iteration():
+            for q in range(N):
+                eng.backward(model(xs[q]).float().pow(2).mean(), q)
+            eng.step()
+        for _ in range(args.warmup):
+            iteration()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            iteration()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out["overlap" if overlap else "serial"] = e0.elapsed_time(e1) / args.steps
+        out["launched_during_backward"] = eng.launched_during_backward
+        phi = eng.plan.phi
+        del eng, model
+        torch.cuda.empty_cache()
+    line = {"impl": "gb300", "metric": "ZeRO engine training iteration (4 virtual ranks)",
+            "value": 1e3 / out["overlap"], "unit": "iterations/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": out["overlap"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "ToyModel hidden 1024 x12 + Linear(1024,10), round-robin N=4",
+                       "phi": phi, "tokens_per_rank": args.tokens, "bucket_elems": args.bucket,
+                       "ms_per_iteration": {"serial": out["serial"], "overlap": out["overlap"]},
+                       "bucket_launches_during_backward": out["launched_during_backward"]}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,6 +706,10 @@ def main(argv=None):
     ap.add_argument("--prefetch", type=int, default=0,
                     help="ZeRO-3 stream through zero_zero3_pass with this many layer buffers "
                          "(gathers on a second stream); 0 = serial Python loop")
+    ap.add_argument("--engine", action="store_true",
+                    help="time a training iteration through the autograd-driven engine")
+    ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")
+    ap.add_argument("--bucket", type=int, default=5_000_000, help="--engine: bucket elements")
     ap.add_argument("--layer-states", type=int, default=40,
                     help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")
     args = ap.parse_args(argv)
@@ -657,6 +720,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.engine:
+        return run_engine(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 
