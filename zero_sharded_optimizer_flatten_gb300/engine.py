@@ -80,6 +80,7 @@ class ZeroEngine:
                     parts.append((b, cnt))
             self._tensor_buckets.append(parts)
         self.reduction_stream = torch.cuda.Stream(dev) if overlap_comm else None
+        self._reduce = Z.ReduceScatterRange(plan, self.grads, op, self.grad_shards)
         self.step_count = 0
         self.launched_during_backward = 0
         self._current: Optional[int] = None
@@ -115,12 +116,11 @@ class ZeroEngine:
     def _launch(self, b: int):
         lo, hi = self.buckets[b]
         if self.reduction_stream is None:
-            Z.zero_reduce_scatter_range(self.plan, self.grads, self.op, self.grad_shards, lo, hi)
+            self._reduce(lo, hi)
         else:
             # the replica copies were queued on the current stream
             self.reduction_stream.wait_stream(torch.cuda.current_stream())
-            Z.zero_reduce_scatter_range(self.plan, self.grads, self.op, self.grad_shards, lo, hi,
-                                        stream=self.reduction_stream)
+            self._reduce(lo, hi, stream=self.reduction_stream)
         self._launched[b] = True
 
     # ------------------------------------------------------------------

@@ -637,3 +637,33 @@ def zero_reduce_scatter_range(plan: Plan, grads, op, grad_shards, flat_lo: int, 
     op_i = _OPS[op] if isinstance(op, str) else int(op)
     _check(L.zero_reduce_scatter_range(plan.handle, _ptrs(g), dt, op_i, _ptrs(out), mask,
                                        int(flat_lo), int(flat_hi), _stream(stream)))
+
+
+class ReduceScatterRange:
+    """A prepared zero_reduce_scatter_range: the pointer arrays of one set of
+    replicas and shards are marshalled once; each call passes a flat range
+    (a bucket) and a stream."""
+
+    def __init__(self, plan: Plan, grads, op, grad_shards, rank_mask=None, dtype=None):
+        torch = _torch()
+        L = lib()
+        vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+        L.zero_reduce_scatter_range.argtypes = [vp, vpp, ctypes.c_int, ctypes.c_int, vpp,
+                                                ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64,
+                                                vp]
+        L.zero_reduce_scatter_range.restype = ctypes.c_int
+        self.plan = plan
+        self.mask = _mask(plan, rank_mask)
+        self.dt = _sixteen(grads) if dtype is None else dtype
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        ext = plan.flat_extent(self.mask)
+        self._g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
+        self._out = _ptrs(_per_rank(plan, grad_shards, "grad_shards", self.mask, torch.float32))
+        self.op = _OPS[op] if isinstance(op, str) else int(op)
+        self._keep = (grads, grad_shards)
+
+    def __call__(self, flat_lo: int, flat_hi: int, stream=None):
+        _check(lib().zero_reduce_scatter_range(self.plan.handle, self._g, self.dt, self.op,
+                                               self._out, self.mask, int(flat_lo), int(flat_hi),
+                                               _stream(stream)))
