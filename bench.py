@@ -505,6 +505,19 @@ def run_gpu(args, world, rank, local):
               for _ in range(args.steps)]
     else:
         ev = [pair() for _ in range(args.steps)]
+    graph = None
+    if args.graph:
+        # capture the K timed steps (each with its own step number) into one
+        # CUDA graph and replay it once: no host work between the launches
+        if args.flush_l2 or w.zero3:
+            raise SystemExit("--graph times back-to-back flat steps only")
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            for k in range(args.steps):
+                run.step(t + 1 + k)
+        torch.cuda.synchronize(dev)
     flush = None
     if args.flush_l2:
         # a buffer twice the size of L2, rewritten before every timed step
@@ -516,11 +529,15 @@ def run_gpu(args, world, rank, local):
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for k in range(args.steps):
-        t += 1
-        if flush is not None:
-            flush.fill_(k & 0xFF)
-        run.step(t, ev[k])
+    if graph is not None:
+        graph.replay()
+        t += args.steps
+    else:
+        for k in range(args.steps):
+            t += 1
+            if flush is not None:
+                flush.fill_(k & 0xFF)
+            run.step(t, ev[k])
     stop.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -539,6 +556,9 @@ def run_gpu(args, world, rank, local):
     elif w.zero3:
         kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
         bytes_per_launch = run.kernel_bytes
+    elif graph is not None:
+        kernel_s = elapsed / args.steps   # graph replay: launches back to back
+        bytes_per_launch = run.bytes_per_step
     else:
         kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
         bytes_per_launch = run.bytes_per_step
@@ -583,6 +603,9 @@ def run_gpu(args, world, rank, local):
             "l2": (f"flushed: a 256 MB buffer is rewritten before every timed step, outside "
                    f"the step's events ({run.bytes_per_step / 1e6:.1f} MB touched per step)"
                    if args.flush_l2 else
+                   f"back to back in a CUDA graph; {run.bytes_per_step / 1e6:.1f} MB touched "
+                   f"per step ({'fits' if run.bytes_per_step < 120e6 else 'larger than'} L2)"
+                   if args.graph else
                    f"inputs larger than L2: {run.bytes_per_step / 1e9:.2f} GB touched per step"),
             "hbm_gbs_per_step": run.bytes_per_step / (elapsed / args.steps) / 1e9,
         },
@@ -721,6 +744,8 @@ def main(argv=None):
     ap.add_argument("--flush-l2", action="store_true",
                     help="rewrite a 256 MB buffer before every timed step (for groups that fit "
                          "in L2); the steps are then timed by their own events")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps into one CUDA graph and replay it")
     ap.add_argument("--engine", action="store_true",
                     help="time a training iteration through the autograd-driven engine")
     ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")
