@@ -506,17 +506,19 @@ def run_gpu(args, world, rank, local):
     else:
         ev = [pair() for _ in range(args.steps)]
     graph = None
-    if args.graph:
+    graph_launches = 0
+    use_graph = args.graph and not args.flush_l2 and not w.zero3
+    if use_graph:
         # capture the K timed steps (each with its own step number) into one
         # CUDA graph and replay it once: no host work between the launches
-        if args.flush_l2 or w.zero3:
-            raise SystemExit("--graph times back-to-back flat steps only")
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
+        n0 = Z.zero_launch_count()
         with torch.cuda.graph(graph, stream=cap):
             for k in range(args.steps):
                 run.step(t + 1 + k)
+        graph_launches = Z.zero_launch_count() - n0   # kernel nodes the replay runs
         torch.cuda.synchronize(dev)
     flush = None
     if args.flush_l2:
@@ -541,7 +543,7 @@ def run_gpu(args, world, rank, local):
     stop.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
-    launches = Z.zero_launch_count() - launches0
+    launches = Z.zero_launch_count() - launches0 + graph_launches
     barrier(dist, local)
     clocks.stop()
     elapsed = start.elapsed_time(stop) / 1e3
@@ -605,9 +607,12 @@ def run_gpu(args, world, rank, local):
                    if args.flush_l2 else
                    f"back to back in a CUDA graph; {run.bytes_per_step / 1e6:.1f} MB touched "
                    f"per step ({'fits' if run.bytes_per_step < 120e6 else 'larger than'} L2)"
-                   if args.graph else
+                   if use_graph else
                    f"inputs larger than L2: {run.bytes_per_step / 1e9:.2f} GB touched per step"),
             "hbm_gbs_per_step": run.bytes_per_step / (elapsed / args.steps) / 1e9,
+            "launch": ("the K timed steps captured in one CUDA graph (each with its own step "
+                       "number), replayed once" if use_graph else
+                       "one Python call per step through the binding"),
         },
         "roofline": {
             "bound": "hbm",
@@ -744,8 +749,9 @@ def main(argv=None):
     ap.add_argument("--flush-l2", action="store_true",
                     help="rewrite a 256 MB buffer before every timed step (for groups that fit "
                          "in L2); the steps are then timed by their own events")
-    ap.add_argument("--graph", action="store_true",
-                    help="capture the timed steps into one CUDA graph and replay it")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every timed step from Python instead of replaying the "
+                         "steps captured in one CUDA graph (the default for flat groups)")
     ap.add_argument("--engine", action="store_true",
                     help="time a training iteration through the autograd-driven engine")
     ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")
