@@ -153,13 +153,18 @@ class ClockSampler:
 # helpers
 
 
+# The files that define the kernels and their launch shape; host-only code
+# (argument checks, the plan, other entry points) does not change them.
+KERNEL_FILES = ("zero_internal.h", "zero_kernels.cuh", "zero_kernels_bf16.cu",
+                "zero_kernels_fp16.cu", "zero_launch.cu")
+
+
 def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "zero_sharded_optimizer_flatten_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_FILES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
