@@ -667,6 +667,77 @@ def run_gpu(args, world, rank, local):
     return 0
 
 
+def run_offload_cpu(args, world, rank, local):
+    """ZeRO-Offload with the CPU optimizer: per step the GPU reduce-scatters
+    the 8 replicas into pinned host fp32 shards, host threads run AdamW on the
+    host-resident state, the GPU all-gathers the host 16-bit shards into HBM.
+    Timed on the host clock (part of the step runs on the CPU)."""
+    import torch
+
+    import zero_sharded_optimizer_flatten_gb300 as Z
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+    S = [plan.shard_len(r) for r in range(w.n_ranks)]
+    p16 = W.params16(w, dev)
+    full16 = torch.zeros_like(p16)
+    dm = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+    Z.zero_init_shards(plan, p16, dm, [torch.empty_like(x) for x in dm],
+                       [torch.empty_like(x) for x in dm])
+    torch.cuda.synchronize(dev)
+    master = [x.cpu().pin_memory() for x in dm]
+    del dm
+    pin = lambda n, dt: torch.zeros(n, dtype=dt, pin_memory=True)  # noqa: E731
+    m = [pin(n, torch.float32) for n in S]
+    v = [pin(n, torch.float32) for n in S]
+    gsh = [pin(n, torch.float32) for n in S]
+    s16 = [pin(n, w.torch_dtype) for n in S]
+    grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+    hp = Z.AdamW()
+    dt = Z.ZERO_BF16 if w.dtype == "bf16" else Z.ZERO_FP16
+    phases = {"reduce": 0.0, "cpu_adamw": 0.0, "gather": 0.0}
+
+    def one(t, acc=None):
+        t0 = time.perf_counter()
+        Z.zero_reduce_scatter(plan, grads, w.op, gsh)
+        Z.zero_sync()
+        t1 = time.perf_counter()
+        Z.zero_cpu_adamw_shard_step(plan, master, m, v, gsh, s16, hp, t, dt,
+                                    n_threads=args.threads)
+        t2 = time.perf_counter()
+        Z.zero_allgather(plan, s16, full16)
+        Z.zero_sync()
+        t3 = time.perf_counter()
+        if acc is not None:
+            acc["reduce"] += t1 - t0
+            acc["cpu_adamw"] += t2 - t1
+            acc["gather"] += t3 - t2
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        one(t)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t += 1
+        one(t, phases)
+    el = time.perf_counter() - t0
+    line = {"impl": "gb300", "metric": METRIC, "value": plan.phi * args.steps / el, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.title, "phi": plan.phi,
+                       "offload": "CPU optimizer: fp32 state in pinned host memory, AdamW on "
+                                  f"{args.threads if args.threads > 0 else os.cpu_count()} host "
+                                  "threads, GPU reduce-scatter and all-gather across the host link",
+                       "ms_per_phase": {k: 1e3 * x / args.steps for k, x in phases.items()},
+                       "timing": "host clock, device synchronised at each phase"}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_engine(args, world, rank, local):
     """A training iteration of the ToyModel group (hidden 1024, 12 layers,
     round-robin over 4 virtual ranks) through the autograd-driven engine:
@@ -757,6 +828,10 @@ def main(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every timed step from Python instead of replaying the "
                          "steps captured in one CUDA graph (the default for flat groups)")
+    ap.add_argument("--offload-cpu", action="store_true",
+                    help="ZeRO-Offload with the CPU optimizer (host threads run AdamW)")
+    ap.add_argument("--threads", type=int, default=0,
+                    help="--offload-cpu: host threads (0 = all hardware threads)")
     ap.add_argument("--engine", action="store_true",
                     help="time a training iteration through the autograd-driven engine")
     ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")
@@ -773,6 +848,8 @@ def main(argv=None):
         return run_reference(args, world, rank)
     if args.engine:
         return run_engine(args, world, rank, local)
+    if args.offload_cpu:
+        return run_offload_cpu(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 

@@ -215,6 +215,23 @@ zero_status zero_adamw_shard_step(const zero_plan* plan, float* const* master, f
                                   uint64_t rank_mask, void* stream);
 
 /*
+ * ZeRO-Offload's CPU optimizer ([ZeRO-2 blog] §4.5: offload_optimizer to the
+ * CPU, DeepSpeedCPUAdam, pinned buffers): the update of
+ * zero_adamw_shard_step computed by host threads on HOST buffers (master, m,
+ * v, grad_shards and out16_shard are host memory, pinned or not), with the
+ * same binary32 operations in the same order, so the results equal the GPU
+ * update bit for bit.  It runs only when called: the usual offload step is
+ * zero_reduce_scatter into pinned host grad_shards, zero_sync, this call,
+ * then zero_allgather from the pinned host 16-bit shards.  Synchronous;
+ * n_threads <= 0 uses every hardware thread.
+ */
+zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* const* master,
+                                      float* const* m, float* const* v,
+                                      const float* const* grad_shards, void* const* out16_shard,
+                                      zero_dtype dtype, const zero_adamw_hparams* hp,
+                                      int64_t step, uint64_t rank_mask, int32_t n_threads);
+
+/*
  * All-gather ([ZeRO-2 blog] §4.4): full_flat16[f] = shards16[r][i] for every
  * (f, i) owned by a rank in rank_mask.  Flat-mode tail padding belongs to
  * the last rank's shard and is copied like any other element.

@@ -355,3 +355,33 @@ def test_optimizer_state_in_host_memory():
         assert torch.equal(dev_case.master[r].cpu(), hm[r])
         assert torch.equal(dev_case.m[r].cpu(), hmm[r]) and torch.equal(dev_case.v[r].cpu(), hv[r])
     assert torch.equal(dev_case.full16, full)
+
+
+def test_cpu_optimizer_offload_pipeline():
+    """ZeRO-Offload with the CPU optimizer: the GPU reduce-scatters into pinned
+    host fp32 shards, host threads run AdamW on host-resident state, the GPU
+    all-gathers the host 16-bit shards.  Bit-identical to the fused step."""
+    w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    dev_case = Case(w, with_oracle=False)
+    plan = dev_case.plan
+    S = [plan.shard_len(r) for r in range(4)]
+    pin = lambda n, dt: torch.zeros(n, dtype=dt, pin_memory=True)  # noqa: E731
+    hm = [dev_case.master[r].cpu().pin_memory() for r in range(4)]
+    hmm = [pin(n, torch.float32) for n in S]
+    hv = [pin(n, torch.float32) for n in S]
+    hg = [pin(n, torch.float32) for n in S]
+    h16 = [pin(n, w.torch_dtype) for n in S]
+    full = torch.zeros_like(dev_case.full16)
+    for t in (1, 2, 3):
+        g = dev_case.grads(t)
+        Z.zero_step(plan, g, "avg", dev_case.master, dev_case.m, dev_case.v, dev_case.full16, None,
+                    HP, t)
+        Z.zero_reduce_scatter(plan, g, "avg", hg)
+        Z.zero_sync()
+        Z.zero_cpu_adamw_shard_step(plan, hm, hmm, hv, hg, h16, HP, t, Z.ZERO_BF16)
+        Z.zero_allgather(plan, h16, full)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(dev_case.master[r].cpu(), hm[r])
+        assert torch.equal(dev_case.v[r].cpu(), hv[r])
+    assert torch.equal(dev_case.full16, full)

@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <atomic>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "zero_capi_util.h"
@@ -27,6 +28,20 @@ char* error_buffer() {
 }
 
 std::atomic<int64_t> g_launches{0};
+
+// The binary32 constants of step t, each formed in binary64 and rounded once.
+StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t) {
+  StepScalars s;
+  s.d = static_cast<float>(1.0 - h.lr * h.weight_decay);
+  s.b1 = static_cast<float>(h.beta1);
+  s.b2 = static_cast<float>(h.beta2);
+  s.c1 = static_cast<float>(1.0 - h.beta1);
+  s.c2 = static_cast<float>(1.0 - h.beta2);
+  s.ss = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
+  s.sb = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
+  s.eps = static_cast<float>(h.eps);
+  return s;
+}
 
 namespace {
 
@@ -78,20 +93,6 @@ zero_status check_hparams(const char* fn, const zero_adamw_hparams* hp, int64_t 
     return fail(ZERO_ERR_INVALID, "%s: betas must lie in [0, 1)", fn);
   if (step < 1) return fail(ZERO_ERR_INVALID, "%s: step must be >= 1 (got %" PRId64 ")", fn, step);
   return ZERO_OK;
-}
-
-// The binary32 constants of step t, each formed in binary64 and rounded once.
-StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t) {
-  StepScalars s;
-  s.d = static_cast<float>(1.0 - h.lr * h.weight_decay);
-  s.b1 = static_cast<float>(h.beta1);
-  s.b2 = static_cast<float>(h.beta2);
-  s.c1 = static_cast<float>(1.0 - h.beta1);
-  s.c2 = static_cast<float>(1.0 - h.beta2);
-  s.ss = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
-  s.sb = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
-  s.eps = static_cast<float>(h.eps);
-  return s;
 }
 
 void set_scale(LaunchArgs& a, int n_ranks, zero_reduce_op op) {
@@ -344,6 +345,71 @@ extern "C" zero_status zero_adamw_shard_step(const zero_plan* plan, float* const
   }
   a.sc = make_scalars(*hp, step);
   return run_buckets(fn, Kind::kAdamw, dtype, plan, rank_mask, 0, a, stream);
+}
+
+extern "C" zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* const* master,
+                                                 float* const* m, float* const* v,
+                                                 const float* const* grad_shards,
+                                                 void* const* out16_shard, zero_dtype dtype,
+                                                 const zero_adamw_hparams* hp, int64_t step,
+                                                 uint64_t rank_mask, int32_t n_threads) {
+  const char* fn = "zero_cpu_adamw_shard_step";
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  ZERO_TRY(check_hparams(fn, hp, step));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  if (out16_shard) ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, true));
+  const StepScalars sc = make_scalars(*hp, step);
+  // the masked ranks' shards as one list of pieces of at most `chunk` elements
+  int64_t total = 0;
+  for (int r = 0; r < plan->n_ranks; ++r)
+    if (in_mask(rank_mask, r)) total += plan->shard_len[r];
+  int nt = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+  if (nt < 1) nt = 1;
+  const int64_t chunk = std::max<int64_t>(4096, (total + nt - 1) / nt);
+  struct Piece {
+    int r;
+    int64_t off, len;
+  };
+  std::vector<Piece> pieces;
+  try {
+    for (int r = 0; r < plan->n_ranks; ++r) {
+      if (!in_mask(rank_mask, r)) continue;
+      for (int64_t off = 0; off < plan->shard_len[r]; off += chunk)
+        pieces.push_back({r, off, std::min(chunk, plan->shard_len[r] - off)});
+    }
+  } catch (const std::bad_alloc&) {
+    return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  }
+  auto work = [&](size_t first) {
+    for (size_t j = first; j < pieces.size(); j += static_cast<size_t>(nt)) {
+      const Piece& pc = pieces[j];
+      uint16_t* o = out16_shard && out16_shard[pc.r]
+                        ? static_cast<uint16_t*>(out16_shard[pc.r]) + pc.off
+                        : nullptr;
+      cpu_adamw_range(sc, dtype, master[pc.r] + pc.off, m[pc.r] + pc.off, v[pc.r] + pc.off,
+                      grad_shards[pc.r] + pc.off, o, pc.len);
+    }
+  };
+  nt = static_cast<int>(std::min<size_t>(static_cast<size_t>(nt), pieces.size()));
+  if (nt <= 1) {
+    work(0);
+    return ZERO_OK;
+  }
+  std::vector<std::thread> threads;
+  try {
+    for (int k = 1; k < nt; ++k) threads.emplace_back(work, static_cast<size_t>(k));
+  } catch (const std::exception&) {
+    for (auto& th : threads) th.join();
+    return fail(ZERO_ERR_OOM, "%s: could not start host threads", fn);
+  }
+  work(0);
+  for (auto& th : threads) th.join();
+  return ZERO_OK;
 }
 
 extern "C" zero_status zero_allgather(const zero_plan* plan, const void* const* shards16,

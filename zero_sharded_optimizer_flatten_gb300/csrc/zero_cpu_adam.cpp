@@ -1,0 +1,56 @@
+// Host-side AdamW of the offloaded optimizer (ZeRO-Offload's CPU optimizer):
+// the element loop the host threads of zero_cpu_adamw_shard_step run.  It
+// performs the same binary32 operations in the same order as the GPU update
+// (compiled with -ffp-contract=off, so no operation is fused into an FMA;
+// division and square root are the IEEE ones), so both give identical bits.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+// Round to nearest even on the upper half of the binary32 pattern; NaN stays
+// a quiet NaN with its sign.
+inline uint16_t to_bf16(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x0040u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+inline uint16_t to_fp16(float x) {
+  const _Float16 h = static_cast<_Float16>(x);  // IEEE conversion, nearest even
+  uint16_t r;
+  memcpy(&r, &h, 2);
+  return r;
+}
+
+}  // namespace
+
+void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* __restrict p,
+                     float* __restrict m, float* __restrict v, const float* __restrict g,
+                     uint16_t* __restrict out16, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float gi = g[i];
+    float pp = p[i] * s.d;
+    const float mm = s.b1 * m[i] + s.c1 * gi;
+    const float vv = s.b2 * v[i] + s.c2 * (gi * gi);
+    const float den = sqrtf(vv) / s.sb + s.eps;
+    pp = pp - s.ss * (mm / den);
+    p[i] = pp;
+    m[i] = mm;
+    v[i] = vv;
+  }
+  if (!out16) return;
+  if (dtype == ZERO_BF16) {
+    for (int64_t i = 0; i < n; ++i) out16[i] = to_bf16(p[i]);
+  } else {
+    for (int64_t i = 0; i < n; ++i) out16[i] = to_fp16(p[i]);
+  }
+}
+
+}  // namespace zero

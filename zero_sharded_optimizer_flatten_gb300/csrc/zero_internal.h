@@ -104,6 +104,13 @@ struct AmpParams {
   zero_adamw_hparams hp;
 };
 
+// The binary32 constants of step t (zero_capi.cpp).
+StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t);
+
+// AdamW + cast over n elements of host memory (zero_cpu_adam.cpp).
+void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m, float* v,
+                     const float* g, uint16_t* out16, int64_t n);
+
 // Host launchers of the mixed-precision helpers (zero_launch.cu).
 int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
                         AmpBcast* bcast, const AmpParams& p, void* stream);

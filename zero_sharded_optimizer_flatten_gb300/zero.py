@@ -667,3 +667,56 @@ class ReduceScatterRange:
         _check(lib().zero_reduce_scatter_range(self.plan.handle, self._g, self.dt, self.op,
                                                self._out, self.mask, int(flat_lo), int(flat_hi),
                                                _stream(stream)))
+
+
+def _host_addr(a, what):
+    """Address of a host array (numpy, CPU tensor) or an int."""
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{what}: array must be contiguous")
+        return a.ctypes.data
+    torch = _torch()
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError(f"{what}: expected a contiguous host tensor")
+        return a.data_ptr()
+    raise TypeError(f"{what}: expected a numpy array, a host tensor or an int address")
+
+
+def zero_cpu_adamw_shard_step(plan: Plan, master, m, v, grad_shards, out16_shard, hparams: AdamW,
+                              step: int, dtype: int, rank_mask=None, n_threads: int = 0):
+    """ZeRO-Offload's CPU optimizer: AdamW + cast by host threads on host
+    buffers (lists of n_ranks host arrays; entries of unmasked ranks ignored)."""
+    L = lib()
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    L.zero_cpu_adamw_shard_step.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, ctypes.c_int,
+                                            ctypes.POINTER(AdamWHparams), ctypes.c_int64,
+                                            ctypes.c_uint64, ctypes.c_int32]
+    L.zero_cpu_adamw_shard_step.restype = ctypes.c_int
+    mask = _mask(plan, rank_mask)
+
+    def arr(seq, what, nullable=False):
+        if seq is None:
+            return None
+        if len(seq) != plan.n_ranks:
+            raise ValueError(f"{what}: expected {plan.n_ranks} entries")
+        vals = []
+        for r, a in enumerate(seq):
+            if not (mask >> r) & 1 or (a is None and nullable):
+                vals.append(0)
+                continue
+            n = a.size if isinstance(a, np.ndarray) else (a.numel() if hasattr(a, "numel") else None)
+            if n is not None and n < plan.shard_len(r):
+                raise ValueError(f"{what}[{r}]: {n} elements, needs {plan.shard_len(r)}")
+            vals.append(_host_addr(a, f"{what}[{r}]"))
+        return _ptrs(vals)
+    hp = hparams.c()
+    o16 = arr(out16_shard, "out16_shard", nullable=True)
+    _check(L.zero_cpu_adamw_shard_step(plan.handle, arr(master, "master"), arr(m, "m"),
+                                       arr(v, "v"), arr(grad_shards, "grad_shards"), o16,
+                                       int(dtype), ctypes.byref(hp), int(step), mask,
+                                       int(n_threads)))
