@@ -172,3 +172,10 @@ def test_binding_checks_sizes_before_the_library():
     with pytest.raises(ValueError):
         Z.zero_step(plan, [cpu, cpu], "avg", [None] * 2, [None] * 2, [None] * 2, None, None,
                     Z.AdamW(), 1)
+
+
+def test_binding_exports_every_declared_call(L):
+    """The Python package exposes every C call under its C name."""
+    import zero_sharded_optimizer_flatten_gb300 as pkg
+    for n in _declared():
+        assert hasattr(pkg, n), f"the binding lacks {n}"

@@ -720,3 +720,39 @@ def zero_cpu_adamw_shard_step(plan: Plan, master, m, v, grad_shards, out16_shard
                                        arr(v, "v"), arr(grad_shards, "grad_shards"), o16,
                                        int(dtype), ctypes.byref(hp), int(step), mask,
                                        int(n_threads)))
+
+
+# ----------------------------------------------------------------------------
+# the plan queries under their C names (the Plan object caches the same data)
+
+
+def zero_plan_total(plan: Plan):
+    """(phi, padded)."""
+    return plan.phi, plan.padded
+
+
+def zero_plan_info(plan: Plan):
+    """(n_ranks, mode, align_elems, n_tensors)."""
+    return plan.n_ranks, plan.mode, plan.align, len(plan.numel)
+
+
+def zero_plan_shard(plan: Plan, rank: int):
+    """(flat_off, len) of rank `rank`'s shard (flat_off -1 in round-robin mode)."""
+    return plan._shard(rank)
+
+
+def zero_plan_segments(plan: Plan, rank: int) -> np.ndarray:
+    """Rows (tensor_idx, tensor_off, flat_off, shard_off, len)."""
+    return plan.segments(rank)
+
+
+def zero_plan_describe(plan: Plan) -> str:
+    return plan.describe()
+
+
+def zero_plan_destroy(plan: Plan):
+    """Release the plan now (it is otherwise released when collected)."""
+    h = plan._h
+    if h is not None and h.value:
+        lib().zero_plan_destroy(h)
+    plan._h = None
