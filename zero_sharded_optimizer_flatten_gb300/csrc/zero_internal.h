@@ -12,7 +12,10 @@
 namespace zero {
 
 constexpr int kMaxRanks = 64;     // rank_mask is a uint64_t
-constexpr int kThreads = 256;     // threads per CTA of every kernel
+#ifndef ZERO_THREADS
+#define ZERO_THREADS 256
+#endif
+constexpr int kThreads = ZERO_THREADS;  // threads per CTA of every kernel
 constexpr int kVec = 4;           // elements per quad (8 B of 16-bit, 16 B of fp32 data)
 constexpr int kHalf = kThreads * kVec;  // 1024: distance between a thread's two quads
 constexpr int kTile = 2 * kHalf;  // 2048 elements per CTA per tile
