@@ -527,8 +527,10 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize(dev)
     flush = None
     if args.flush_l2:
-        # a buffer twice the size of L2, rewritten before every timed step
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        # a buffer twice the size of L2, read (not written, which would leave
+        # dirty lines to be written back during the step) before every step
+        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        flush_sink = torch.empty((), dtype=torch.float32, device=dev)
     barrier(dist, local)
     torch.cuda.synchronize(dev)
     launches0 = Z.zero_launch_count()
@@ -543,7 +545,7 @@ def run_gpu(args, world, rank, local):
         for k in range(args.steps):
             t += 1
             if flush is not None:
-                flush.fill_(k & 0xFF)
+                torch.sum(flush, out=flush_sink)
             run.step(t, ev[k])
     stop.record(stream)
     torch.cuda.synchronize(dev)
@@ -607,7 +609,7 @@ def run_gpu(args, world, rank, local):
             "virtual_ranks": w.n_ranks,
             "storage": f"{w.dtype} params and gradients, fp32 master/m/v",
             "parallelism": f"{world} independent replica(s); {w.n_ranks} virtual ranks each",
-            "l2": (f"flushed: a 256 MB buffer is rewritten before every timed step, outside "
+            "l2": (f"flushed: a 256 MB buffer is read before every timed step, outside "
                    f"the step's events ({run.bytes_per_step / 1e6:.1f} MB touched per step)"
                    if args.flush_l2 else
                    f"back to back in a CUDA graph; {run.bytes_per_step / 1e6:.1f} MB touched "
@@ -823,7 +825,7 @@ def main(argv=None):
                     help="ZeRO-3 stream through zero_zero3_pass with this many layer buffers "
                          "(gathers on a second stream); 0 = serial Python loop")
     ap.add_argument("--flush-l2", action="store_true",
-                    help="rewrite a 256 MB buffer before every timed step (for groups that fit "
+                    help="read a 256 MB buffer before every timed step (for groups that fit "
                          "in L2); the steps are then timed by their own events")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every timed step from Python instead of replaying the "
