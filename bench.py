@@ -545,7 +545,7 @@ def run_gpu(args, world, rank, local):
         for k in range(args.steps):
             t += 1
             if flush is not None:
-                torch.sum(flush, out=flush_sink)
+                torch.sum(flush, dim=0, out=flush_sink)
             run.step(t, ev[k])
     stop.record(stream)
     torch.cuda.synchronize(dev)
