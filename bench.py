@@ -740,6 +740,76 @@ def run_offload_cpu(args, world, rank, local):
     return 0
 
 
+def run_unfused(args, world, rank, local):
+    """The three unfused calls of one step (zero_reduce_scatter,
+    zero_adamw_shard_step with 16-bit shard output, zero_allgather), each
+    timed by its own CUDA events, with its algorithmic bytes per element:
+    reduce 2N + 4, AdamW 4 + 24 + 2, gather 2 + 2."""
+    import torch
+
+    import zero_sharded_optimizer_flatten_gb300 as Z
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+    S = [plan.shard_len(r) for r in range(w.n_ranks)]
+    p16 = W.params16(w, dev)
+    full = torch.zeros_like(p16)
+    master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+    m = [torch.empty_like(x) for x in master]
+    v = [torch.empty_like(x) for x in master]
+    Z.zero_init_shards(plan, p16, master, m, v)
+    gsh = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
+    s16 = [torch.empty(n, dtype=w.torch_dtype, device=dev) for n in S]
+    grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+    hp = Z.AdamW()
+    E = plan.padded
+    per = {"k_reduce_scatter": 2 * w.n_ranks + 4, "k_adamw": 30, "k_allgather": 4}
+
+    def pair():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = {k: [pair() for _ in range(args.steps)] for k in per}
+    t = 0
+    for k in range(args.warmup + args.steps):
+        t += 1
+        rec = k >= args.warmup
+        i = k - args.warmup
+        if rec:
+            ev["k_reduce_scatter"][i][0].record()
+        Z.zero_reduce_scatter(plan, grads, w.op, gsh)
+        if rec:
+            ev["k_reduce_scatter"][i][1].record()
+            ev["k_adamw"][i][0].record()
+        Z.zero_adamw_shard_step(plan, master, m, v, gsh, s16, hp, t)
+        if rec:
+            ev["k_adamw"][i][1].record()
+            ev["k_allgather"][i][0].record()
+        Z.zero_allgather(plan, s16, full)
+        if rec:
+            ev["k_allgather"][i][1].record()
+    torch.cuda.synchronize(dev)
+    peak, _ = measured_peaks()
+    kernels = {}
+    total = 0.0
+    for k, b in per.items():
+        sec = statistics.fmean(a.elapsed_time(c) for a, c in ev[k]) / 1e3
+        total += sec
+        kernels[k] = {"us": 1e6 * sec, "bytes": b * E, "GB/s": b * E / sec / 1e9,
+                      "frac": b * E / sec / 1e9 / peak}
+    line = {"impl": "gb300", "metric": METRIC, "value": plan.phi / total, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.title, "phi": plan.phi,
+                       "path": "unfused: reduce-scatter, AdamW + cast, all-gather",
+                       "kernels": kernels,
+                       "bytes_per_element": sum(per.values())}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_engine(args, world, rank, local):
     """A training iteration of the ToyModel group (hidden 1024, 12 layers,
     round-robin over 4 virtual ranks) through the autograd-driven engine:
@@ -830,6 +900,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every timed step from Python instead of replaying the "
                          "steps captured in one CUDA graph (the default for flat groups)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the three unfused calls of a step separately")
     ap.add_argument("--offload-cpu", action="store_true",
                     help="ZeRO-Offload with the CPU optimizer (host threads run AdamW)")
     ap.add_argument("--threads", type=int, default=0,
@@ -852,6 +924,8 @@ def main(argv=None):
         return run_engine(args, world, rank, local)
     if args.offload_cpu:
         return run_offload_cpu(args, world, rank, local)
+    if args.unfused:
+        return run_unfused(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 
