@@ -415,11 +415,51 @@ __device__ __forceinline__ double block_sum(double x) {
   return t;
 }
 
+// Binary64 sum of x over the block without a block-wide barrier: every warp
+// reduces its lanes and parks the result in shared memory; the warp that
+// arrives last (shared-memory counter) adds the warps' sums in index order and
+// returns the total in its lane 0 (valid == true there).  The order of the
+// additions is fixed, so the result does not depend on which warp is last.
+// The counter must be zero on entry; it is zero again on exit.
+__device__ __forceinline__ double warp_tree_sum(double x, double* warp_part, int* arrived,
+                                               bool& valid) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int last = 0;
+  if (lane == 0) {
+    warp_part[warp] = x;
+    __threadfence_block();
+    last = atomicAdd(arrived, 1) == kThreads / 32 - 1;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  valid = false;
+  if (!last) return 0.0;
+  __threadfence_block();
+  double t = 0.0;
+  if (lane == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
+    *arrived = 0;
+    valid = true;
+  }
+  return t;
+}
+
 // Reduce-scatter into fp32 shards plus, per tile, the binary64 sum of the
 // binary32 squares of the reduced gradient (a thread adds its up to 8
 // squares in binary32 first).  A non-finite gradient makes the sum non-finite.
+// One tile per CTA (the usual launch): the per-tile sum needs no barrier
+// (warp_tree_sum); if the grid ever strides over several tiles, the block-wide
+// barrier version is used.
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
+  __shared__ double warp_part[kThreads / 32];
+  __shared__ int arrived;
+  const bool one_tile = static_cast<int64_t>(gridDim.x) >= a.n_tiles;
+  if (one_tile) {
+    if (threadIdx.x == 0) arrived = 0;
+    __syncthreads();
+  }
   for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
     const Job& jb = a.jobs[find_job(a, tile)];
     const int64_t base = (tile - jb.tile_begin) * kTile;
@@ -446,8 +486,14 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
         }
       }
     }
-    const double t = block_sum<kThreads>(static_cast<double>(s));
-    if (threadIdx.x == 0) a.partials[a.tile_base + tile] = t;
+    if (one_tile) {
+      bool valid;
+      const double t = warp_tree_sum(static_cast<double>(s), warp_part, &arrived, valid);
+      if (valid) a.partials[a.tile_base + tile] = t;
+    } else {
+      const double t = block_sum<kThreads>(static_cast<double>(s));
+      if (threadIdx.x == 0) a.partials[a.tile_base + tile] = t;
+    }
   }
 }
 
