@@ -670,6 +670,8 @@ extern "C" zero_status zero_sync(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ZERO_ERR_CUDA, "zero_sync: %s", cudaGetErrorString(e));
+  if (ZERO_STEP_TMA != 0 && take_device_error())
+    return fail(ZERO_ERR_TIMEOUT, "zero_sync: a kernel gave up waiting for its staged copies");
   return ZERO_OK;
 }
 

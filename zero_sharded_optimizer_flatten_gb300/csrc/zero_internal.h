@@ -21,6 +21,17 @@ constexpr int kHalf = kThreads * kVec;  // 1024: distance between a thread's two
 constexpr int kTile = 2 * kHalf;  // 2048 elements per CTA per tile
 constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 
+// Fused step through bulk-copy (TMA) staging: 0 never; 1 whenever every job
+// of the launch has 8-element-aligned offsets and length; 2 only for launches
+// of at most ZERO_TMA_MAX_TILES tiles (small groups, which one wave of the
+// plain kernel cannot pipeline).
+#ifndef ZERO_STEP_TMA
+#define ZERO_STEP_TMA 0
+#endif
+#ifndef ZERO_TMA_MAX_TILES
+#define ZERO_TMA_MAX_TILES 4096
+#endif
+
 // Resident CTAs per SM the kernels are compiled for (caps registers at 64),
 // and the grid: ZERO_GRID_MULT = 0 launches one CTA per tile; k > 0 caps the
 // grid at k times the resident capacity (the CTAs then stride over tiles).
@@ -81,6 +92,7 @@ struct LaunchArgs {
   double* partials;                // mixed-precision: per-tile binary64 sums of squares
   int64_t tile_base;               // index of this launch's first tile among the step's
   const struct AmpBcast* bcast;    // mixed-precision: copies of the decision record
+  int* err;                        // device error word (a bounded wait gave up)
   Job jobs[kMaxJobs];
 };
 
@@ -113,6 +125,11 @@ StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t);
 // AdamW + cast over n elements of host memory (zero_cpu_adam.cpp).
 void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m, float* v,
                      const float* g, uint16_t* out16, int64_t n);
+
+// Address of the device error word on the current device (nullptr on
+// failure), and read-and-clear of it (zero_launch.cu).
+int* device_error_word();
+int take_device_error();
 
 // Host launchers of the mixed-precision helpers (zero_launch.cu).
 int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,

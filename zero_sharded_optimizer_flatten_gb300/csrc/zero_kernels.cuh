@@ -588,8 +588,20 @@ struct PickStats {
 };
 
 template <class T>
+int launch_step_tma(const LaunchArgs& a, cudaStream_t s);
+
+template <class T>
 int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
   const void* fn = nullptr;
+  if (kind == Kind::kStep && ZERO_STEP_TMA != 0 && a.n_ranks >= 1 && a.n_ranks <= 8 &&
+      (ZERO_STEP_TMA == 1 || a.n_tiles <= ZERO_TMA_MAX_TILES)) {
+    bool eligible = true;
+    for (int j = 0; j < a.n_jobs && eligible; ++j) {
+      const Job& jb = a.jobs[j];
+      eligible = jb.vec && jb.flat_off % 8 == 0 && jb.shard_off % 8 == 0 && jb.len % 8 == 0;
+    }
+    if (eligible) return launch_step_tma<T>(a, s);
+  }
   switch (kind) {
     case Kind::kStep: fn = by_ranks<T, PickStep>(a.n_ranks); break;
     case Kind::kReduceScatter: fn = by_ranks<T, PickReduce>(a.n_ranks); break;

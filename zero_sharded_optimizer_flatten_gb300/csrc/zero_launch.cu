@@ -133,8 +133,61 @@ int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* str
   return static_cast<int>(cudaGetLastError());
 }
 
+int tma_grid(const void* fn, int smem_bytes, int64_t n_tiles) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({fn, dev});
+  if (it == cache.end()) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+        cudaSuccess)
+      return -1;
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem_bytes) !=
+        cudaSuccess)
+      return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -1;
+    it = cache.emplace(std::make_pair(fn, dev), (per_sm > 0 ? per_sm : 1) * sms).first;
+  }
+  return static_cast<int>(n_tiles < it->second ? n_tiles : it->second);
+}
+
+// The device error word: set by a kernel whose bounded wait gave up.
+static __device__ int g_device_error;
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static std::mutex mu;
+  static int* ptr[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
+int take_device_error() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (v) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  }
+  return v;
+}
+
 int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ZERO_STEP_TMA != 0 && kind == Kind::kStep && !a.err) {
+    LaunchArgs& w = const_cast<LaunchArgs&>(a);
+    w.err = device_error_word();
+  }
   if (dtype == ZERO_BF16) return launch_typed<__nv_bfloat16>(kind, a, s);
   return launch_typed<__half>(kind, a, s);
 }
