@@ -61,7 +61,7 @@ typedef enum {
   ZERO_ERR_ALIGN = 2,       /* a device pointer is not 16-byte aligned           */
   ZERO_ERR_CUDA = 3,        /* CUDA runtime error (launch or asynchronous)       */
   ZERO_ERR_OOM = 4,         /* host allocation failed                            */
-  ZERO_ERR_TIMEOUT = 5,     /* reserved: no call waits on the device             */
+  ZERO_ERR_TIMEOUT = 5,     /* a bounded wait on the device gave up (zero_sync)   */
   ZERO_ERR_UNSUPPORTED = 6  /* valid request this build does not implement       */
 } zero_status;
 
@@ -406,8 +406,20 @@ zero_status zero_step_amp_noalloc(const zero_plan* plan, const void* const* grad
                                   void* d_state, uint64_t rank_mask, int64_t bucket_elems,
                                   void* stream);
 
-/* Synchronize `stream` and report any asynchronous device error. */
+/* Synchronize `stream` and report any asynchronous device error, and
+ * ZERO_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check
+ * (the device error word is then cleared). */
 zero_status zero_sync(void* stream);
+
+/*
+ * Self-test of the timeout path: one kernel waits on a barrier that nothing
+ * ever completes, gives up after limit_ns nanoseconds (1e3 .. 1e10) and
+ * raises the device error word, so the next zero_sync(stream) returns
+ * ZERO_ERR_TIMEOUT.  No fault and no hang: the context stays usable.  The
+ * library's only waiting kernels (the optional bulk-copy staging of the
+ * fused step) give up the same way, after one second.
+ */
+zero_status zero_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* zero_last_error(void);

@@ -179,3 +179,10 @@ def test_binding_exports_every_declared_call(L):
     import zero_sharded_optimizer_flatten_gb300 as pkg
     for n in _declared():
         assert hasattr(pkg, n), f"the binding lacks {n}"
+
+
+def test_selftest_rejects_bad_limits(L):
+    before = Z.zero_launch_count()
+    for bad in (0, 999, 10**11):
+        assert L.zero_selftest_wait_timeout(bad, None) == Z.ZERO_ERR_INVALID
+    assert Z.zero_launch_count() == before

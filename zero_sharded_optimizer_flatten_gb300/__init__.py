@@ -14,5 +14,5 @@ from .zero import (AMP_STATE_BYTES, ZERO_BF16, ZERO_FP16, ZERO_PART_FLAT,  # noq
                    zero_plan_describe, zero_plan_destroy, zero_plan_info, zero_plan_partitions,
                    zero_plan_segments, zero_plan_shard, zero_plan_total, zero_reduce_scatter,
                    zero_reduce_scatter_range,
-                   zero_step, zero_step_amp, zero_step_amp_noalloc, zero_sync, zero_version,
-                   zero_zero3_pass)
+                   zero_selftest_wait_timeout, zero_step, zero_step_amp, zero_step_amp_noalloc,
+                   zero_sync, zero_version, zero_zero3_pass)

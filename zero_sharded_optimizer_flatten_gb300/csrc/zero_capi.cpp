@@ -241,6 +241,7 @@ extern "C" zero_status zero_init_shards(const zero_plan* plan, const void* full_
                                         zero_dtype dtype, float* const* master, float* const* m,
                                         float* const* v, uint64_t rank_mask, void* stream) {
   const char* fn = "zero_init_shards";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -268,6 +269,7 @@ extern "C" zero_status zero_reduce_scatter(const zero_plan* plan, const void* co
                                            float* const* grad_shards, uint64_t rank_mask,
                                            int64_t bucket_elems, void* stream) {
   const char* fn = "zero_reduce_scatter";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -291,6 +293,7 @@ extern "C" zero_status zero_reduce_scatter_range(const zero_plan* plan, const vo
                                                  float* const* grad_shards, uint64_t rank_mask,
                                                  int64_t flat_lo, int64_t flat_hi, void* stream) {
   const char* fn = "zero_reduce_scatter_range";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -322,6 +325,7 @@ extern "C" zero_status zero_adamw_shard_step(const zero_plan* plan, float* const
                                              const zero_adamw_hparams* hp, int64_t step,
                                              uint64_t rank_mask, void* stream) {
   const char* fn = "zero_adamw_shard_step";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -354,6 +358,7 @@ extern "C" zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* c
                                                  const zero_adamw_hparams* hp, int64_t step,
                                                  uint64_t rank_mask, int32_t n_threads) {
   const char* fn = "zero_cpu_adamw_shard_step";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -416,6 +421,7 @@ extern "C" zero_status zero_allgather(const zero_plan* plan, const void* const* 
                                       zero_dtype dtype, void* full_flat16, uint64_t rank_mask,
                                       void* stream) {
   const char* fn = "zero_allgather";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -439,6 +445,7 @@ extern "C" zero_status zero_step(const zero_plan* plan, const void* const* grads
                                  int64_t step, uint64_t rank_mask, int64_t bucket_elems,
                                  void* stream) {
   const char* fn = "zero_step";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -471,6 +478,7 @@ extern "C" zero_status zero_step(const zero_plan* plan, const void* const* grads
 
 extern "C" zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream) {
   const char* fn = "zero_amp_init";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_amp_config(fn, cfg));
   if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
@@ -509,6 +517,7 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
                                      int64_t workspace_bytes, uint64_t rank_mask,
                                      int64_t bucket_elems, void* stream) {
   const char* fn = "zero_step_amp";
+  NvtxRange nvtx_range(fn);
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
@@ -602,6 +611,7 @@ extern "C" zero_status zero_zero3_pass(const zero_plan* plan, const zero_layer* 
                                        const zero_adamw_hparams* hp, int64_t step,
                                        void* gather_stream, void* step_stream) {
   const char* fn = "zero_zero3_pass";
+  NvtxRange nvtx_range(fn);
   clear_error();
   if (!plan) return fail(ZERO_ERR_INVALID, "%s: plan is NULL", fn);
   const uint64_t all = plan->n_ranks >= 64 ? ~UINT64_C(0) : ((UINT64_C(1) << plan->n_ranks) - 1);
@@ -670,8 +680,22 @@ extern "C" zero_status zero_sync(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ZERO_ERR_CUDA, "zero_sync: %s", cudaGetErrorString(e));
-  if (ZERO_STEP_TMA != 0 && take_device_error())
-    return fail(ZERO_ERR_TIMEOUT, "zero_sync: a kernel gave up waiting for its staged copies");
+  if (take_device_error(stream))
+    return fail(ZERO_ERR_TIMEOUT, "zero_sync: a kernel gave up a bounded wait on the device");
+  return ZERO_OK;
+}
+
+extern "C" zero_status zero_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  const char* fn = "zero_selftest_wait_timeout";
+  clear_error();
+  if (limit_ns < 1000 || limit_ns > INT64_C(10000000000))
+    return fail(ZERO_ERR_INVALID, "%s: limit_ns must lie in [1e3, 1e10]", fn);
+  ZERO_TRY(pending_error(fn));
+  const int err = launch_selftest_wait(limit_ns, stream);
+  if (err != 0)
+    return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
+                cudaGetErrorString(static_cast<cudaError_t>(err)));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return ZERO_OK;
 }
 

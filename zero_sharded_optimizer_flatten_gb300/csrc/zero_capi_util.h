@@ -1,6 +1,7 @@
 // Status and error-message helpers shared by the C-ABI translation units.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -23,5 +24,14 @@ inline zero_status fail(zero_status st, const char* fmt, ...) {
   va_end(ap);
   return st;
 }
+
+// An NVTX range named after the C-ABI call, for timelines in Nsight tools
+// (a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace zero

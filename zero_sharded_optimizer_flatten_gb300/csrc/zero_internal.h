@@ -129,7 +129,10 @@ void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m,
 // Address of the device error word on the current device (nullptr on
 // failure), and read-and-clear of it (zero_launch.cu).
 int* device_error_word();
-int take_device_error();
+int take_device_error(void* stream);
+
+// Launch the bounded-wait self-test kernel (zero_launch.cu).
+int launch_selftest_wait(int64_t limit_ns, void* stream);
 
 // Host launchers of the mixed-precision helpers (zero_launch.cu).
 int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,

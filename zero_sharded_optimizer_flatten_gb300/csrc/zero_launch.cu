@@ -6,6 +6,7 @@
 #include <utility>
 
 #include "zero_kernels.cuh"
+#include "zero_kernels_tma.cuh"
 
 namespace zero {
 
@@ -172,14 +173,39 @@ int* device_error_word() {
   return ptr[dev];
 }
 
-int take_device_error() {
+int take_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_device_error, sizeof v, 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return 0;
   if (v) {
     const int zero = 0;
-    cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                s) == cudaSuccess)
+      cudaStreamSynchronize(s);
   }
   return v;
+}
+
+// The failure path of a bounded wait, on purpose: wait on a barrier that no
+// thread ever arrives at, give up after limit_ns, raise the error word.
+__global__ void k_selftest_wait(int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait_bounded(b, 0, limit_ns) && err) atomicExch(err, 1);
+}
+
+int launch_selftest_wait(int64_t limit_ns, void* stream) {
+  int* err = device_error_word();
+  if (!err) return static_cast<int>(cudaErrorUnknown);
+  k_selftest_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      err, static_cast<unsigned long long>(limit_ns));
+  return static_cast<int>(cudaGetLastError());
 }
 
 int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream) {

@@ -756,3 +756,12 @@ def zero_plan_destroy(plan: Plan):
     if h is not None and h.value:
         lib().zero_plan_destroy(h)
     plan._h = None
+
+
+def zero_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Launch the timeout self-test kernel; the next zero_sync raises
+    ZeroError with status ZERO_ERR_TIMEOUT (see include/zero.h)."""
+    L = lib()
+    L.zero_selftest_wait_timeout.argtypes = [ctypes.c_int64, ctypes.c_void_p]
+    L.zero_selftest_wait_timeout.restype = ctypes.c_int
+    _check(L.zero_selftest_wait_timeout(int(limit_ns), _stream(stream)))
