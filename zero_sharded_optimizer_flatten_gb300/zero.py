@@ -88,6 +88,20 @@ def lib():
                 "zero_step": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vp, vpp, hp,
                               i64, u64, i64, vp],
                 "zero_sync": [vp],
+                "zero_selftest_wait_timeout": [i64, vp],
+                "zero_reduce_scatter_range": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, u64, i64,
+                                              i64, vp],
+                "zero_cpu_adamw_shard_step": [vp, vpp, vpp, vpp, vpp, vpp, ctypes.c_int, hp, i64,
+                                              u64, i32],
+                "zero_amp_init": [vp, ctypes.POINTER(AmpConfigC), vp],
+                "zero_amp_workspace_bytes": [vp, u64, i64, i64p],
+                "zero_step_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp, vp,
+                                  vpp, hp, ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
+                "zero_step_amp_noalloc": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp,
+                                          vpp, vp, vpp, hp, ctypes.POINTER(AmpConfigC), vp, u64,
+                                          i64, vp],
+                "zero_zero3_pass": [vp, ctypes.POINTER(_LayerC), i32, vpp, i32, ctypes.c_int,
+                                    ctypes.c_int, hp, i64, vp, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
