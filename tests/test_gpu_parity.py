@@ -385,3 +385,23 @@ def test_cpu_optimizer_offload_pipeline():
         assert torch.equal(dev_case.master[r].cpu(), hm[r])
         assert torch.equal(dev_case.v[r].cpu(), hv[r])
     assert torch.equal(dev_case.full16, full)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_non_finite_gradients_propagate_like_the_oracle(dtype):
+    """+inf, -inf and NaN in one replica: the plain step propagates them as
+    IEEE arithmetic does, on the same elements as the oracle (the update
+    with overflow checks is zero_step_amp)."""
+    w = W.small((4096, 37), 4, mode="flat", align=16, dtype=dtype, op="avg")
+    c = Case(w)
+    g = c.grads(1)
+    g[2][10] = float("inf")
+    g[2][11] = float("-inf")
+    g[1][12] = float("nan")
+    g[0][13] = float("inf")
+    g[3][13] = float("-inf")          # inf + -inf -> NaN
+    Z.zero_step(c.plan, g, "avg", c.master, c.m, c.v, c.full16, None, HP, 1)
+    c.oracle_step(g, 1, hp_oracle(HP))
+    torch.cuda.synchronize()
+    c.compare("non-finite")
+    assert np.isnan(f32(c.master[0])[10:14]).all()
