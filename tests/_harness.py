@@ -57,19 +57,13 @@ def key16(x: np.ndarray) -> np.ndarray:
     return np.where(x & 0x8000, -(x & 0x7FFF), x)
 
 
-def is_nan16(x: np.ndarray, dtype_code: int = None) -> np.ndarray:
-    """NaN patterns of binary16 (exponent 0x1f) and bfloat16 (exponent 0xff):
-    both formats are covered by testing the top 9 bits below the sign for the
-    bfloat16 layout and the top 6 for binary16; callers pass the dtype when
-    they know it."""
+def is_nan16(x: np.ndarray, dtype_code: int) -> np.ndarray:
+    """NaN bit patterns of binary16 (dtype_code 0: exponent field 0x1f) or
+    bfloat16 (dtype_code 1: exponent field 0xff), non-zero mantissa."""
     x = x.astype(np.int64)
-    nan_bf16 = ((x & 0x7F80) == 0x7F80) & ((x & 0x007F) != 0)
-    nan_fp16 = ((x & 0x7C00) == 0x7C00) & ((x & 0x03FF) != 0)
     if dtype_code == 0:
-        return nan_fp16
-    if dtype_code == 1:
-        return nan_bf16
-    return nan_bf16 & nan_fp16
+        return ((x & 0x7C00) == 0x7C00) & ((x & 0x03FF) != 0)
+    return ((x & 0x7F80) == 0x7F80) & ((x & 0x007F) != 0)
 
 
 def assert_16_close(got: np.ndarray, ref: np.ndarray, what: str, ulps: int = ULP16,
