@@ -44,6 +44,10 @@ constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 #ifndef ZERO_GRID_MULT
 #define ZERO_GRID_MULT 0
 #endif
+// 256-byte L2 prefetch hints on the streaming loads (tuning switch).
+#ifndef ZERO_L2_PREFETCH
+#define ZERO_L2_PREFETCH 0
+#endif
 
 // Binary32 constants of one AdamW step, formed on the host in binary64 and
 // rounded once each (see zero_adamw_hparams).

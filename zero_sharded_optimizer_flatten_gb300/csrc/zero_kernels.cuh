@@ -97,10 +97,16 @@ __device__ __forceinline__ uint2 pack4(const float* x) {
 // instruction), which keeps the DRAM request stream dense.
 
 // Gradient replicas and shard copies are read exactly once: non-coherent
-// path, no L1 allocation.
+// path, no L1 allocation (ZERO_L2_PREFETCH adds a 256-byte L2 prefetch hint).
 __device__ __forceinline__ uint2 ld_once8(const void* p) {
   uint2 r;
+#if ZERO_L2_PREFETCH
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];"
+      : "=r"(r.x), "=r"(r.y)
+      : "l"(p));
+#else
   asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+#endif
   return r;
 }
 
@@ -111,7 +117,16 @@ __device__ __forceinline__ uint16_t ld_once16(const void* p) {
 }
 
 __device__ __forceinline__ float4 ld_state(const float* p) {
+#if ZERO_L2_PREFETCH
+  float4 r;
+  asm volatile("ld.global.cs.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+#else
   return __ldcs(reinterpret_cast<const float4*>(p));
+#endif
 }
 
 __device__ __forceinline__ void st_state(float* p, const float4& v) {
