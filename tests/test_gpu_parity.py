@@ -266,10 +266,12 @@ def test_llama7b_rank0_shard_full_size_sampled():
     assert _sampled(W.WORKLOADS["llama7b_rank0"], 3, n_random=8000) > 8000
 
 
-def test_llama13b_zero3_layer_pass_sampled():
-    """Two layers of the ZeRO-3 stream: all-gather 8 bf16 shards into the
-    layer buffer (bit-exact), then the fused step writing each rank's shard."""
-    w = W.WORKLOADS["llama13b_layer"]
+@pytest.mark.parametrize("key", ["llama13b_layer", "llama13b_full_layer"])
+def test_llama13b_zero3_layer_pass_sampled(key):
+    """Two layers of the ZeRO-3 stream (the 3 MLP matrices, or the whole
+    decoder layer): all-gather 8 bf16 shards into the layer buffer
+    (bit-exact), then the fused step writing each rank's shard."""
+    w = W.WORKLOADS[key]
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
     L = W.flat_len(w)
     S = plan.shard_len(0)

@@ -126,7 +126,8 @@ def test_flat_plan_configs():
     """The five parameter groups: sizes from the published shapes."""
     expect = {"tiny_mlp": (1053706, 1053760, 263440), "bert_base": (109482240, 109482240,
               13685280), "llama7b_rank0": (6738415616, 6738415616, 842301952),
-              "llama13b_layer": (212336640, 212336640, 26542080)}
+              "llama13b_layer": (212336640, 212336640, 26542080),
+              "llama13b_full_layer": (317204480, 317204480, 39650560)}
     for key, (phi, P, S) in expect.items():
         w = W.WORKLOADS[key]
         assert oracle.plan_flat(list(w.numel), w.n_ranks, w.align) == (phi, P, S)

@@ -113,6 +113,12 @@ def llama13b_mlp_numel(hidden=5120, ffn=13824):
     return [ffn * hidden, ffn * hidden, hidden * ffn]
 
 
+def llama13b_layer_numel(hidden=5120, ffn=13824):
+    """A whole LLaMA-13B decoder layer: q, k, v, o, gate, up, down, 2 norms."""
+    h = hidden
+    return [h * h] * 4 + [ffn * h, ffn * h, h * ffn] + [h, h]
+
+
 WORKLOADS = {
     "tiny_mlp": Workload(
         "tiny_mlp", "tiny MLP 2x[Linear(256,1024)+Linear(1024,256)]+Linear(256,10), fp16, "
@@ -134,6 +140,10 @@ WORKLOADS = {
         "llama13b_layer", "ZeRO-3 pass over 40 LLaMA-13B MLP layers (212M each), N=8 flat, "
         "bf16, averaged", tuple(llama13b_mlp_numel()), 8, "flat", 16, "bf16", "avg", 0.02,
         1e-3, steps=1, layers=40, zero3=True, seed=1239),
+    "llama13b_full_layer": Workload(
+        "llama13b_full_layer", "ZeRO-3 pass over 40 whole LLaMA-13B decoder layers (317M each), "
+        "N=8 flat, bf16, averaged", tuple(llama13b_layer_numel()), 8, "flat", 16, "bf16", "avg",
+        0.02, 1e-3, steps=1, layers=40, zero3=True, seed=1240),
 }
 
 
