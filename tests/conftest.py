@@ -8,3 +8,26 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a); run on the GPU host")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word(request):
+    """After every GPU test: zero_sync() must report no device-side error (a
+    bounded wait that gave up, or, in a bounds-checked build, an index that
+    fell outside its buffer)."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    try:
+        import torch
+    except ImportError:
+        return
+    if not torch.cuda.is_available():
+        return
+    from zero_sharded_optimizer_flatten_gb300 import zero as Z
+    if Z._lib is None:
+        return
+    Z.zero_sync()

@@ -165,10 +165,17 @@ zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs&
   return ZERO_OK;
 }
 
+// The buffer lengths the bounds-checked build verifies every access against.
+void set_bounds(LaunchArgs& a, const zero_plan* plan) {
+  a.flat_len = plan->padded;
+  for (int r = 0; r < plan->n_ranks; ++r) a.shard_len[r] = plan->shard_len[r];
+}
+
 // Run `kind` bucket by bucket over the flat index space.
 zero_status run_buckets(const char* fn, Kind kind, zero_dtype dtype, const zero_plan* plan,
                         uint64_t mask, int64_t bucket, LaunchArgs& a, void* stream,
                         int64_t* tiles_done = nullptr) {
+  set_bounds(a, plan);
   std::vector<Job> jobs;
   const int64_t total = plan->padded;
   const int64_t B = bucket > 0 ? bucket : std::max<int64_t>(total, 1);
@@ -312,6 +319,7 @@ extern "C" zero_status zero_reduce_scatter_range(const zero_plan* plan, const vo
     if (in_mask(rank_mask, r)) a.gshard[r] = grad_shards[r];
   }
   set_scale(a, plan->n_ranks, op);
+  set_bounds(a, plan);
   std::vector<Job> jobs;
   build_jobs(plan, rank_mask, flat_lo, flat_hi, jobs);
   if (jobs.empty()) return ZERO_OK;
@@ -680,7 +688,11 @@ extern "C" zero_status zero_sync(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ZERO_ERR_CUDA, "zero_sync: %s", cudaGetErrorString(e));
-  if (take_device_error(stream))
+  const int dev_err = take_device_error(stream);
+  if (dev_err == kErrBounds)
+    return fail(ZERO_ERR_INVALID, "zero_sync: a kernel index fell outside its buffer "
+                                  "(bounds-checked build)");
+  if (dev_err)
     return fail(ZERO_ERR_TIMEOUT, "zero_sync: a kernel gave up a bounded wait on the device");
   return ZERO_OK;
 }

@@ -44,6 +44,15 @@ constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 #ifndef ZERO_GRID_MULT
 #define ZERO_GRID_MULT 0
 #endif
+// Bounds-checked build: every kernel access is checked against the plan's
+// buffer lengths; a violation skips the access and sets the device error
+// word to 2 (zero_sync reports it).
+#ifndef ZERO_DEBUG_BOUNDS
+#define ZERO_DEBUG_BOUNDS 0
+#endif
+constexpr int kErrTimeout = 1;
+constexpr int kErrBounds = 2;
+
 // 256-byte L2 prefetch hints on the streaming loads (tuning switch).
 #ifndef ZERO_L2_PREFETCH
 #define ZERO_L2_PREFETCH 0
@@ -96,7 +105,9 @@ struct LaunchArgs {
   double* partials;                // mixed-precision: per-tile binary64 sums of squares
   int64_t tile_base;               // index of this launch's first tile among the step's
   const struct AmpBcast* bcast;    // mixed-precision: copies of the decision record
-  int* err;                        // device error word (a bounded wait gave up)
+  int* err;                        // device error word (bounded wait, bounds check)
+  int64_t flat_len;                // bounds-checked builds: length of the flat buffers
+  int64_t shard_len[kMaxRanks];    // bounds-checked builds: shard lengths
   Job jobs[kMaxJobs];
 };
 

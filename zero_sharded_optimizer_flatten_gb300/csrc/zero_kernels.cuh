@@ -254,6 +254,21 @@ __device__ __forceinline__ int find_job(const LaunchArgs& a, int64_t tile) {
   return lo;
 }
 
+// Bounds-checked builds: are the n elements at job offset e inside the flat
+// buffer and inside the rank's shard?  Otherwise raise the error word.
+__device__ __forceinline__ bool access_ok(const LaunchArgs& a, const Job& jb, int64_t e,
+                                          int64_t n) {
+#if ZERO_DEBUG_BOUNDS
+  const int64_t f = jb.flat_off + e, i = jb.shard_off + e;
+  if (jb.rank < 0 || jb.rank >= kMaxRanks || f < 0 || f + n > a.flat_len || i < 0 ||
+      i + n > a.shard_len[jb.rank] || e + n > jb.len) {
+    if (a.err) atomicExch(a.err, kErrBounds);
+    return false;
+  }
+#endif
+  return true;
+}
+
 // Calls body_vec(job, e0, two) for the thread's quads at job offsets e0 and
 // e0 + kHalf (the second only when `two`), or body_one(job, e) for single
 // elements, over every tile of the launch.
@@ -265,12 +280,16 @@ __device__ __forceinline__ void for_each_tile(const LaunchArgs& a, BodyVec body_
     const int64_t base = (tile - jb.tile_begin) * kTile;
     if (jb.vec) {
       const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
-      if (e0 < jb.len) body_vec(jb, e0, e0 + kHalf < jb.len);
+      if (e0 < jb.len) {
+        const bool two = e0 + kHalf < jb.len;
+        if (access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec)))
+          body_vec(jb, e0, two);
+      }
     } else {
 #pragma unroll 1
       for (int k = 0; k < kTile / kThreads; ++k) {
         const int64_t e = base + k * kThreads + threadIdx.x;
-        if (e < jb.len) body_one(jb, e);
+        if (e < jb.len && access_ok(a, jb, e, 1)) body_one(jb, e);
       }
     }
   }
@@ -481,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
     float s = 0.f;
     if (jb.vec) {
       const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
-      if (e0 < jb.len) {
-        const bool two = e0 + kHalf < jb.len;
+      const bool two = e0 + kHalf < jb.len;
+      if (e0 < jb.len && access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec))) {
         const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
         float g[8];
         reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
 #pragma unroll 1
       for (int k = 0; k < kTile / kThreads; ++k) {
         const int64_t e = base + k * kThreads + threadIdx.x;
-        if (e < jb.len) {
+        if (e < jb.len && access_ok(a, jb, e, 1)) {
           const float g = reduce1<T, NR>(a, jb.flat_off + e);
           a.gshard[jb.rank][jb.shard_off + e] = g;
           s = __fadd_rn(s, __fmul_rn(g, g));

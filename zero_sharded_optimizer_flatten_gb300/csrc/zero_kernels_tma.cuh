@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_step_tma(const __grid_constant_
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
     const int64_t f = jb.flat_off + base, i = jb.shard_off + base;
+    if (!access_ok(a, jb, base, cnt)) return;  // bounds-checked builds only
 #pragma unroll
     for (int q = 0; q < NR; ++q)
       bulk_g2s(dst + q * kTile * 2, static_cast<const uint16_t*>(a.grads[q]) + f,

@@ -210,7 +210,7 @@ int launch_selftest_wait(int64_t limit_ns, void* stream) {
 
 int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (ZERO_STEP_TMA != 0 && kind == Kind::kStep && !a.err) {
+  if ((ZERO_DEBUG_BOUNDS || (ZERO_STEP_TMA != 0 && kind == Kind::kStep)) && !a.err) {
     LaunchArgs& w = const_cast<LaunchArgs&>(a);
     w.err = device_error_word();
   }
