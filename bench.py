@@ -362,7 +362,10 @@ class FlatRunner:
           direct -- zero_step is given the host buffers; its kernel reads the
                     replicas and writes the parameters across the host link;
           copies -- copy the replicas to HBM, zero_step, copy the result back.
-        Returns {"direct": s, "copies": s} per step and the bytes moved."""
+        A third timing, "h2d_only", copies the replicas to HBM and does nothing
+        else: the host link's own rate, the bound the two paths are held to.
+        Returns {"direct": s, "copies": s, "h2d_only": s} per step and the
+        bytes moved."""
         import torch
         w, Z = self.w, self.Z
         host_g = [torch.empty(self.ext, dtype=w.torch_dtype, pin_memory=True)
@@ -383,9 +386,13 @@ class FlatRunner:
                         self.hp, t, rank_mask=self.mask, bucket_elems=w.bucket_elems)
             host_out.copy_(self.full16, non_blocking=True)
 
+        def h2d_only(t):
+            for q in range(w.n_ranks):
+                dev_g[q].copy_(host_g[q], non_blocking=True)
+
         out = {}
         t = t0
-        for name, one in (("direct", direct), ("copies", copies)):
+        for name, one in (("direct", direct), ("copies", copies), ("h2d_only", h2d_only)):
             for _ in range(2):
                 t += 1
                 one(t)
@@ -576,12 +583,16 @@ def run_gpu(args, world, rank, local):
     if not w.zero3 and not args.amp and not args.offload:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         per_step, h2d, d2h = run.e2e(t, e2e_steps)
+        link_s = per_step.pop("h2d_only")
         best = min(per_step, key=per_step.get)
         sec = max_over_ranks(dist, per_step[best], local)
         e2e = {"value": run.elems * world / sec, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "path": best,
                "ms_per_step": {k: 1e3 * v for k, v in per_step.items()},
+               # the inputs must cross the host link: its copy rate bounds the step
+               "link": {"h2d_gbs": h2d / link_s / 1e9, "h2d_ms": 1e3 * link_s,
+                        "frac": link_s / per_step[best]},
                "note": "direct: zero_step reads the pinned host replicas and writes the pinned "
                        "host parameters across NVLink-C2C; copies: cudaMemcpyAsync in, "
                        "zero_step, cudaMemcpyAsync out"}
