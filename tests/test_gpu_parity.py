@@ -211,12 +211,12 @@ def test_zero3_shard_output():
 # full-size groups, sampled parity
 
 
-def _sampled(w: W.Workload, steps: int, hp=HP, n_random=20000):
+def _sampled(w: W.Workload, steps: int, hp=HP, n_random=20000, extra=()):
     """Run the CUDA step at full size and check sampled elements against the
     oracle recomputing those elements one by one from the same inputs."""
-    extra = []
+    extra = list(extra)
     if w.bucket_elems:
-        extra = list(range(0, W.flat_len(w), w.bucket_elems))
+        extra += list(range(0, W.flat_len(w), w.bucket_elems))
     F = sample_indices(w, n_random=n_random, extra=extra)
     rank, shard = owner_of(w, F)
     keep = np.array([(w.mask >> int(r)) & 1 for r in rank], bool) & (rank >= 0)
@@ -250,6 +250,33 @@ def _sampled(w: W.Workload, steps: int, hp=HP, n_random=20000):
     assert_fp32_close(got_v, vv, f"{w.key} v")
     assert_16_close(u16(c.full16[Ft]), out, f"{w.key} full16")
     return F.size
+
+
+# Flat and shard indices past 2^31 and 2^32: every offset the kernels form is
+# 64-bit.  Round-robin groups put a small tensor behind a huge one, so one
+# rank's elements sit at large flat offsets (and, in the first case, rank 0's
+# last tensor at a shard offset past 2^31).  Odd lengths put element-wise
+# jobs there as well as quad jobs.
+LARGE_INDEX = [
+    # numel, rank mask, device bytes needed (replicas, parameters, gathered buffer, state)
+    ((2_200_000_000, 6001, 4003), 0b11, 46 << 30),
+    ((4_300_000_000, 6001), 0b10, 36 << 30),
+]
+
+
+@pytest.mark.parametrize("numel,mask,need", LARGE_INDEX, ids=["past_2^31", "past_2^32"])
+def test_indices_past_32_bits_sampled(numel, mask, need):
+    free, _ = torch.cuda.mem_get_info()
+    if free < need + (4 << 30):
+        pytest.skip(f"needs {need >> 30} GiB of free device memory")
+    w = W.small(numel, 2, mode="round_robin", align=1, dtype="bf16", op="sum", rank_mask=mask)
+    starts = np.concatenate([[0], np.cumsum(np.asarray(numel, np.int64))])
+    extra = list(range(int(starts[1]), int(starts[-1])))        # every small-tensor element
+    for b in (1 << 31, 1 << 32):
+        extra += [x for x in range(b - 4100, b + 4100) if x < starts[-1]]
+    assert _sampled(w, 2, n_random=4000, extra=extra) >= 6001
+    gc.collect()
+    torch.cuda.empty_cache()
 
 
 def test_bert_base_full_size_sampled():
