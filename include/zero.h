@@ -305,7 +305,9 @@ zero_status zero_zero3_pass(const zero_plan* plan, const zero_layer* layers, int
  *  - the gradient replicas carry the loss scale S; they are reduced as by
  *    zero_reduce_scatter into binary32 shards, and the squared L2 norm of
  *    the reduced gradient over every masked rank is accumulated (binary32
- *    squares, binary64 sums, in a fixed order);
+ *    squares; sums in a fixed order with about 48 significant bits, kept as
+ *    pairs of binary32 numbers, squares of 2^64 and above in a second pair
+ *    scaled by 2^-64, so the sum of finite squares is finite);
  *  - a non-finite norm (an inf or NaN anywhere) skips the update: no
  *    parameter, moment or step count changes; if more than one overflow is
  *    still tolerated the tolerance drops by one, else S halves (not below
@@ -348,8 +350,9 @@ typedef struct {
 zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream);
 
 /* Bytes of device workspace zero_step_amp needs for this plan, mask and
- * bucketing: 4 KB of copies of the step's decision record plus one binary64
- * partial sum per 2048-element tile. */
+ * bucketing: an 8 KB head (copies of the step's decision record, the
+ * decision kernel's partial sums) plus one 16-byte partial sum of squares
+ * per 2048-element tile. */
 zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t rank_mask,
                                      int64_t bucket_elems, int64_t* bytes);
 
@@ -361,9 +364,9 @@ zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t rank_mask,
  *  d_state: the device state (read-modify-write);
  *  workspace: caller-owned device scratch of at least
  *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems), 16-byte aligned.
- * Launches the reduction (one launch per bucket), a one-CTA decision kernel
- * and the update; calls must not overlap on the device when they share
- * d_state or workspace.
+ * Launches the reduction (one launch per bucket), the decision kernel and
+ * the update; calls must not overlap on the device when they share d_state
+ * or workspace.
  */
 zero_status zero_step_amp(const zero_plan* plan, const void* const* grads, zero_dtype dtype,
                           zero_reduce_op op, float* const* grad_shards, float* const* master,
@@ -382,12 +385,12 @@ zero_status zero_step_amp(const zero_plan* plan, const void* const* grads, zero_
  * The pages describe no such call; it is a convenience of this library.
  *
  * Same arguments and results as zero_step_amp, minus workspace and
- * workspace_bytes.  The scratch is instead a fixed 1 MiB array compiled into
+ * workspace_bytes.  The scratch is instead a fixed 2 MiB array compiled into
  * the library, present on every GPU that loads it until the process exits;
  * this call allocates nothing (no cudaMalloc, no cudaFree, no allocating
  * library routine).  Limits and rules:
  *  - the step may span at most 130,560 tiles of 2048 elements, i.e.
- *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems) <= 1 MiB (about
+ *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems) <= 2 MiB (about
  *    267 million owned elements per call); larger steps are rejected with
  *    ZERO_ERR_INVALID and a message, and nothing is launched;
  *  - the first call on a device looks up the array's device address with

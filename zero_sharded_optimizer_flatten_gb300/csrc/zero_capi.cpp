@@ -511,8 +511,8 @@ extern "C" zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t 
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   if (!bytes) return fail(ZERO_ERR_INVALID, "%s: bytes is NULL", fn);
-  *bytes = kAmpBcastBytes + count_tiles(plan, rank_mask, bucket_elems) *
-                                static_cast<int64_t>(sizeof(double));
+  *bytes = kAmpHeadBytes + count_tiles(plan, rank_mask, bucket_elems) *
+                                static_cast<int64_t>(sizeof(NormPartial));
   return ZERO_OK;
 }
 
@@ -543,7 +543,7 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
   if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
   if (!aligned16(d_state)) return fail(ZERO_ERR_ALIGN, "%s: d_state is not 16-byte aligned", fn);
   const int64_t tiles = count_tiles(plan, rank_mask, bucket_elems);
-  const int64_t need = kAmpBcastBytes + tiles * static_cast<int64_t>(sizeof(double));
+  const int64_t need = kAmpHeadBytes + tiles * static_cast<int64_t>(sizeof(NormPartial));
   if (!workspace) return fail(ZERO_ERR_INVALID, "%s: workspace is NULL", fn);
   if (!aligned16(workspace)) return fail(ZERO_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
   if (workspace_bytes < need)
@@ -563,18 +563,35 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
     a.shard16[r] = out16_shard ? out16_shard[r] : nullptr;
   }
   a.full16 = full_flat16;
-  // workspace: [decision record copies][one binary64 partial per tile]
-  AmpBcast* bcast = static_cast<AmpBcast*>(workspace);
-  a.bcast = bcast;
-  a.partials = reinterpret_cast<double*>(static_cast<char*>(workspace) + kAmpBcastBytes);
+  // workspace: [AmpHead: decision record copies, decision-kernel sums, beta
+  // powers, counter][one 16-byte sum of squares per tile]
+  AmpHead* head = static_cast<AmpHead*>(workspace);
+  a.head = head;
+  a.bcast = head->bcast;
+  a.partials = reinterpret_cast<NormPartial*>(static_cast<char*>(workspace) + kAmpHeadBytes);
+  a.amp_state = static_cast<const zero_amp_state*>(d_state);
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
   set_scale(a, plan->n_ranks, op);
   int64_t done = 0;
   ZERO_TRY(run_buckets(fn, Kind::kStats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
+  if (done == 0) {
+    // no owned element: one empty reduction launch still prepares the
+    // decision kernel (beta powers, counter)
+    a.n_jobs = 0;
+    a.n_tiles = 0;
+    a.tile_base = 0;
+    const int err = launch_kernel(Kind::kStats, dtype, a, stream);
+    if (err != 0)
+      return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
+                  cudaGetErrorString(static_cast<cudaError_t>(err)));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
   AmpParams p;
   p.cfg = *cfg;
   p.hp = *hp;
   const int err = launch_amp_finalize(a.partials, done, static_cast<zero_amp_state*>(d_state),
-                                      bcast, p, stream);
+                                      head, p, stream);
   if (err != 0)
     return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                 cudaGetErrorString(static_cast<cudaError_t>(err)));

@@ -102,9 +102,12 @@ struct LaunchArgs {
   int32_t n_jobs;
   int32_t pad_;
   int64_t n_tiles;
-  double* partials;                // mixed-precision: per-tile binary64 sums of squares
+  struct NormPartial* partials;    // mixed-precision: per-tile sums of squares
   int64_t tile_base;               // index of this launch's first tile among the step's
   const struct AmpBcast* bcast;    // mixed-precision: copies of the decision record
+  struct AmpHead* head;            // mixed-precision: workspace head (reduction writes)
+  const zero_amp_state* amp_state; // mixed-precision: the device state (step count)
+  double beta1, beta2;             // mixed-precision: AdamW betas
   int* err;                        // device error word (bounded wait, bounds check)
   int64_t flat_len;                // bounds-checked builds: length of the flat buffers
   int64_t shard_len[kMaxRanks];    // bounds-checked builds: shard lengths
@@ -126,9 +129,32 @@ struct alignas(16) AmpBcast {
 };
 static_assert(sizeof(AmpBcast) == 64, "one copy per 64-byte line segment");
 constexpr int kAmpCopies = 64;
-constexpr int64_t kAmpBcastBytes = kAmpCopies * sizeof(AmpBcast);  // head of the workspace
 
-// Parameters of the one-CTA decision kernel of the mixed-precision step.
+// One tile's sum of squared gradients as two unevaluated sums of binary32
+// pairs: a = squares below 2^64, b = the others times 2^-64 (exact scaling),
+// so that no partial sum of finite squares can overflow binary32.  The
+// tile's sum is (a_hi + a_lo) + 2^64 (b_hi + b_lo).
+struct alignas(16) NormPartial {
+  float a_hi, a_lo, b_hi, b_lo;
+};
+static_assert(sizeof(NormPartial) == 16, "one 16-byte store per tile");
+
+// The decision kernel's CTAs (each sums a share of the per-tile partials;
+// the last one to finish adds the CTAs' sums and decides) and their threads.
+constexpr int kFinCtas = 32;
+constexpr int kFinThreads = 256;
+
+// Head of the mixed-precision workspace; the per-tile partials follow it.
+struct alignas(64) AmpHead {
+  AmpBcast bcast[kAmpCopies];        // the decision record, kAmpCopies times
+  NormPartial cta_part[kFinCtas];    // the decision kernel's per-CTA sums
+  double beta_pow[2];                // beta1^t and beta2^t of the step t = step + 1
+  int32_t arrived;                   // decision-kernel CTAs done (reset every step)
+};
+constexpr int64_t kAmpHeadBytes = 8192;
+static_assert(sizeof(AmpHead) <= kAmpHeadBytes, "workspace head");
+
+// Parameters of the decision kernel of the mixed-precision step.
 struct AmpParams {
   zero_amp_config cfg;
   zero_adamw_hparams hp;
@@ -150,8 +176,8 @@ int take_device_error(void* stream);
 int launch_selftest_wait(int64_t limit_ns, void* stream);
 
 // Host launchers of the mixed-precision helpers (zero_launch.cu).
-int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
-                        AmpBcast* bcast, const AmpParams& p, void* stream);
+int launch_amp_finalize(const NormPartial* partials, int64_t n_tiles, zero_amp_state* state,
+                        AmpHead* head, const AmpParams& p, void* stream);
 int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream);
 
 // Host launcher entry (zero_kernels_*.cu): launches `kind` for the jobs in

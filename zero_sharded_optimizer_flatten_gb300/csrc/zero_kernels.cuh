@@ -432,62 +432,139 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_init(const __grid
 // ---------------------------------------------------------------------------
 // mixed-precision controls
 
-// Sum of x over the block in binary64, in a fixed order (shuffle tree inside
-// each warp, then the warps in index order); the result is valid in thread 0.
-template <int NT>
-__device__ __forceinline__ double block_sum(double x) {
-  __shared__ double warp_part[NT / 32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) warp_part[warp] = x;
-  __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < NT / 32; ++w) t += warp_part[w];
-  __syncthreads();
-  return t;
+// Sums of squares in pairs of binary32.
+//
+// GB300 runs binary64 arithmetic at a small fraction of its binary32 rate, so
+// the norm's sums are kept as unevaluated pairs (hi, lo) of binary32 numbers
+// with value hi + lo and |lo| <= ulp(hi)/2.  A pair is extended by Knuth's
+// error-free sum (TwoSum: the rounded sum and its exact rounding error),
+// after which Dekker's Fast2Sum renormalises it; about 48 significant bits
+// survive, and the error-free steps stay exact with gradual underflow.  All
+// terms here are non-negative, so a sum of n terms is within a few times
+// log2(n) * 2^-46 of the exact sum.  A non-finite term leaves the pair
+// non-finite (an inf can turn into a NaN).
+struct Pair {
+  float hi, lo;
+};
+
+__device__ __forceinline__ Pair pair_add(Pair x, Pair y) {
+  const float s = __fadd_rn(x.hi, y.hi);
+  const float bb = __fsub_rn(s, x.hi);
+  const float e = __fadd_rn(__fsub_rn(x.hi, __fsub_rn(s, bb)), __fsub_rn(y.hi, bb));
+  const float t = __fadd_rn(e, __fadd_rn(x.lo, y.lo));
+  const float hi = __fadd_rn(s, t);
+  return {hi, __fsub_rn(t, __fsub_rn(hi, s))};
 }
 
-// Binary64 sum of x over the block without a block-wide barrier: every warp
-// reduces its lanes and parks the result in shared memory; the warp that
-// arrives last (shared-memory counter) adds the warps' sums in index order and
-// returns the total in its lane 0 (valid == true there).  The order of the
-// additions is fixed, so the result does not depend on which warp is last.
-// The counter must be zero on entry; it is zero again on exit.
-__device__ __forceinline__ double warp_tree_sum(double x, double* warp_part, int* arrived,
-                                               bool& valid) {
+__device__ __forceinline__ Pair pair_add1(Pair x, float y) {
+  const float s = __fadd_rn(x.hi, y);
+  const float bb = __fsub_rn(s, x.hi);
+  const float e = __fadd_rn(__fsub_rn(x.hi, __fsub_rn(s, bb)), __fsub_rn(y, bb));
+  const float t = __fadd_rn(e, x.lo);
+  const float hi = __fadd_rn(s, t);
+  return {hi, __fsub_rn(t, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ Pair shfl_down(Pair x, int o) {
+  return {__shfl_down_sync(0xffffffffu, x.hi, o), __shfl_down_sync(0xffffffffu, x.lo, o)};
+}
+
+// A sum of binary32 squares in the two ranges of NormPartial: squares below
+// 2^64 in `a`, the others (and NaNs) times 2^-64 in `b`.  With fewer than
+// 2^40 terms neither pair can overflow unless a square is infinite.
+// (An aggregate, so that it can live in shared memory; start from sq_zero().)
+struct SqSum {
+  Pair a, b;
+
+  __device__ __forceinline__ void add(float sq) {
+    if (sq < 0x1p64f)
+      a = pair_add1(a, sq);
+    else
+      b = pair_add1(b, __fmul_rn(sq, 0x1p-64f));
+  }
+  __device__ __forceinline__ void add(const SqSum& o) {
+    a = pair_add(a, o.a);
+    b = pair_add(b, o.b);
+  }
+  __device__ __forceinline__ void add(const float4& p) {  // a NormPartial as loaded
+    a = pair_add(a, Pair{p.x, p.y});
+    b = pair_add(b, Pair{p.z, p.w});
+  }
+  // The exact value of the two pairs in binary64 (each pair's sum needs at
+  // most 49 bits; the scaling by 2^64 is exact).
+  __device__ __forceinline__ double value() const {
+    return (static_cast<double>(a.hi) + static_cast<double>(a.lo)) +
+           (static_cast<double>(b.hi) + static_cast<double>(b.lo)) * 0x1p64;
+  }
+};
+
+__device__ __forceinline__ SqSum sq_zero() { return SqSum{{0.f, 0.f}, {0.f, 0.f}}; }
+
+// Shuffle tree over the warp (fixed order); the result is valid in lane 0.
+// The `b` range is only reduced when some lane holds a square >= 2^64.
+__device__ __forceinline__ SqSum warp_sum(SqSum s) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  for (int o = 16; o > 0; o >>= 1) s.a = pair_add(s.a, shfl_down(s.a, o));
+  if (__any_sync(0xffffffffu, s.b.hi != 0.f)) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s.b = pair_add(s.b, shfl_down(s.b, o));
+  }
+  return s;
+}
+
+__device__ __forceinline__ void store_partial(NormPartial* p, const SqSum& s) {
+  *reinterpret_cast<float4*>(p) = make_float4(s.a.hi, s.a.lo, s.b.hi, s.b.lo);
+}
+
+// The block's sum of squares without a block-wide barrier: every warp
+// reduces its lanes and parks the result in shared memory; the warp that
+// arrives last (shared-memory counter) adds the warps' sums in index order
+// and stores them to *out from its lane 0.  The order of the additions is
+// fixed, so the result does not depend on which warp is last.  The counter
+// must be zero on entry; it is zero again on exit.
+__device__ __forceinline__ void tile_sum_last_warp(SqSum s, SqSum* warp_part, int* arrived,
+                                                   NormPartial* out) {
+  s = warp_sum(s);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int last = 0;
   if (lane == 0) {
-    warp_part[warp] = x;
+    warp_part[warp] = s;
     __threadfence_block();
     last = atomicAdd(arrived, 1) == kThreads / 32 - 1;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
-  valid = false;
-  if (!last) return 0.0;
+  if (!last) return;
   __threadfence_block();
-  double t = 0.0;
   if (lane == 0) {
-    for (int w = 0; w < kThreads / 32; ++w) t += warp_part[w];
+    SqSum t = warp_part[0];
+    for (int w = 1; w < kThreads / 32; ++w) t.add(warp_part[w]);
     *arrived = 0;
-    valid = true;
+    store_partial(out, t);
   }
-  return t;
 }
 
-// Reduce-scatter into fp32 shards plus, per tile, the binary64 sum of the
-// binary32 squares of the reduced gradient (a thread adds its up to 8
-// squares in binary32 first).  A non-finite gradient makes the sum non-finite.
-// One tile per CTA (the usual launch): the per-tile sum needs no barrier
-// (warp_tree_sum); if the grid ever strides over several tiles, the block-wide
-// barrier version is used.
+// The same with block-wide barriers (CTAs that stride over several tiles).
+__device__ __forceinline__ void tile_sum_barrier(SqSum s, SqSum* warp_part, NormPartial* out) {
+  s = warp_sum(s);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    SqSum t = warp_part[0];
+    for (int w = 1; w < kThreads / 32; ++w) t.add(warp_part[w]);
+    store_partial(out, t);
+  }
+  __syncthreads();
+}
+
+// Reduce-scatter into fp32 shards plus, per tile, the sum of the binary32
+// squares of the reduced gradient (SqSum; a non-finite gradient makes it
+// non-finite).  One tile per CTA (the usual launch): the per-tile sum needs
+// no barrier (tile_sum_last_warp); if the grid ever strides over several
+// tiles, the block-wide barrier version is used.
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
-  __shared__ double warp_part[kThreads / 32];
+  __shared__ SqSum warp_part[kThreads / 32];
   __shared__ int arrived;
   const bool one_tile = static_cast<int64_t>(gridDim.x) >= a.n_tiles;
   if (one_tile) {
@@ -497,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
   for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
     const Job& jb = a.jobs[find_job(a, tile)];
     const int64_t base = (tile - jb.tile_begin) * kTile;
-    float s = 0.f;
+    SqSum s = sq_zero();
     if (jb.vec) {
       const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
       const bool two = e0 + kHalf < jb.len;
@@ -507,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
         reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
         store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) s = __fadd_rn(s, __fmul_rn(g[k], g[k]));
+        for (int k = 0; k < 8; ++k) s.add(__fmul_rn(g[k], g[k]));
       }
     } else {
 #pragma unroll 1
@@ -516,18 +593,26 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
         if (e < jb.len && access_ok(a, jb, e, 1)) {
           const float g = reduce1<T, NR>(a, jb.flat_off + e);
           a.gshard[jb.rank][jb.shard_off + e] = g;
-          s = __fadd_rn(s, __fmul_rn(g, g));
+          s.add(__fmul_rn(g, g));
         }
       }
     }
-    if (one_tile) {
-      bool valid;
-      const double t = warp_tree_sum(static_cast<double>(s), warp_part, &arrived, valid);
-      if (valid) a.partials[a.tile_base + tile] = t;
-    } else {
-      const double t = block_sum<kThreads>(static_cast<double>(s));
-      if (threadIdx.x == 0) a.partials[a.tile_base + tile] = t;
-    }
+    NormPartial* out = a.partials + a.tile_base + tile;
+    if (one_tile)
+      tile_sum_last_warp(s, warp_part, &arrived, out);
+    else
+      tile_sum_barrier(s, warp_part, out);
+  }
+  // The launch holding the step's first tile also prepares the decision
+  // kernel: beta1^t and beta2^t of the step t = step + 1 that an update would
+  // take (binary64 pow, here off the decision's critical path), and a zero
+  // arrival counter.  The decision kernel runs after every launch of this
+  // kernel has completed.
+  if (a.head && a.tile_base == 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+    const double t = static_cast<double>(a.amp_state->step + 1);
+    a.head->beta_pow[0] = pow(a.beta1, t);
+    a.head->beta_pow[1] = pow(a.beta2, t);
+    a.head->arrived = 0;
   }
 }
 
@@ -645,7 +730,8 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kStats: fn = by_ranks<T, PickStats>(a.n_ranks); break;
     case Kind::kAdamwAmp: fn = reinterpret_cast<const void*>(&k_adamw_amp<T>); break;
   }
-  const int grid = grid_for(fn, a.n_tiles);
+  int grid = grid_for(fn, a.n_tiles);
+  if (kind == Kind::kStats && grid == 0) grid = 1;  // an empty launch still prepares the decision
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
   return static_cast<int>(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s));

@@ -39,12 +39,14 @@ int grid_for(const void* fn, int64_t n_tiles) {
   return static_cast<int>(n_tiles < slots ? n_tiles : slots);
 }
 
-// The decision of the mixed-precision step (one CTA): sum the per-tile
-// partials in a fixed order, then update the loss-scale state and form the
-// step's coefficient and AdamW constants (binary64, each rounded once).
-constexpr int kFinalizeThreads = 1024;
+// The decision of the mixed-precision step: sum the per-tile partials in a
+// fixed order (binary32 pairs, see SqSum), then update the loss-scale state
+// and form the step's coefficient and AdamW constants (binary64, each
+// rounded once).  beta1^t and beta2^t come from the reduction kernel.
+constexpr int kFinUnroll = 8;  // partial loads in flight per thread
 
-__device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p) {
+__device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p, double b1t,
+                           double b2t) {
   const double S = x.scale;
   x.norm = sqrt(sumsq) / S;
   if (!isfinite(sumsq)) {
@@ -66,18 +68,17 @@ __device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p) 
     if (q < 1.0) clip = q;
   }
   x.coef = static_cast<float>(clip / S);
-  const int64_t t = x.step + 1;
   const zero_adamw_hparams& h = p.hp;
   x.sc[0] = static_cast<float>(1.0 - h.lr * h.weight_decay);
   x.sc[1] = static_cast<float>(h.beta1);
   x.sc[2] = static_cast<float>(h.beta2);
   x.sc[3] = static_cast<float>(1.0 - h.beta1);
   x.sc[4] = static_cast<float>(1.0 - h.beta2);
-  x.sc[5] = static_cast<float>(h.lr / (1.0 - pow(h.beta1, static_cast<double>(t))));
-  x.sc[6] = static_cast<float>(sqrt(1.0 - pow(h.beta2, static_cast<double>(t))));
+  x.sc[5] = static_cast<float>(h.lr / (1.0 - b1t));
+  x.sc[6] = static_cast<float>(sqrt(1.0 - b2t));
   x.sc[7] = static_cast<float>(h.eps);
   x.overflow = 0;
-  x.step = t;
+  x.step = x.step + 1;
   x.good_steps += 1;
   if (p.cfg.window > 0 && x.good_steps >= p.cfg.window) {
     x.scale = S * 2.0;
@@ -86,46 +87,68 @@ __device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p) 
   }
 }
 
-__global__ void __launch_bounds__(kFinalizeThreads) k_amp_finalize(const double* partials,
-                                                                   int64_t n,
-                                                                   zero_amp_state* st,
-                                                                   AmpBcast* bcast,
-                                                                   const AmpParams p) {
-  // four independent running sums per thread (fixed assignment), then the
-  // block in a fixed order
-  double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
-  constexpr int64_t kStride = 4 * kFinalizeThreads;
-  int64_t i = threadIdx.x;
-  for (; i + 3 * kFinalizeThreads < n; i += kStride) {
-    s0 += __ldcg(partials + i);
-    s1 += __ldcg(partials + i + kFinalizeThreads);
-    s2 += __ldcg(partials + i + 2 * kFinalizeThreads);
-    s3 += __ldcg(partials + i + 3 * kFinalizeThreads);
+// kFinCtas CTAs: CTA c's thread t adds partials j = c*T + t, j + C*T, ... in
+// increasing order; the CTA adds its threads (shuffle trees, then the warps
+// in index order) and publishes its sum; the CTA that arrives last (atomic
+// counter, no waiting) adds the CTAs' sums in index order and decides.
+__global__ void __launch_bounds__(kFinThreads) k_amp_finalize(const NormPartial* partials,
+                                                              int64_t n, zero_amp_state* st,
+                                                              AmpHead* head, const AmpParams p) {
+  constexpr int64_t kAll = static_cast<int64_t>(kFinCtas) * kFinThreads;
+  const float4* src = reinterpret_cast<const float4*>(partials);
+  SqSum s = sq_zero();
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
+  for (; i + (kFinUnroll - 1) * kAll < n; i += kFinUnroll * kAll) {
+    float4 q[kFinUnroll];
+#pragma unroll
+    for (int k = 0; k < kFinUnroll; ++k) q[k] = __ldcg(src + i + k * kAll);
+#pragma unroll
+    for (int k = 0; k < kFinUnroll; ++k) s.add(q[k]);
   }
-  for (; i < n; i += kFinalizeThreads) s0 += __ldcg(partials + i);
-  const double sumsq = block_sum<kFinalizeThreads>((s0 + s1) + (s2 + s3));
-  __shared__ AmpBcast rec;
+  for (; i < n; i += kAll) s.add(__ldcg(src + i));
+  __shared__ SqSum warp_part[kFinThreads / 32];
+  __shared__ int last;
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = s;
+  __syncthreads();
   if (threadIdx.x == 0) {
-    zero_amp_state x = *st;
-    amp_decide(x, sumsq, p);
-    *st = x;
-    AmpBcast b = {};
-    b.overflow = x.overflow;
-    b.coef = x.coef;
-    for (int k = 0; k < 8; ++k) b.sc[k] = x.sc[k];
-    rec = b;
+    SqSum t = warp_part[0];
+    for (int w = 1; w < kFinThreads / 32; ++w) t.add(warp_part[w]);
+    store_partial(&head->cta_part[blockIdx.x], t);
+    __threadfence();
+    last = atomicAdd(&head->arrived, 1) == kFinCtas - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  __shared__ AmpBcast rec;
+  if (threadIdx.x < 32) {
+    SqSum c = sq_zero();
+    if (threadIdx.x < kFinCtas) c.add(__ldcg(reinterpret_cast<const float4*>(head->cta_part) + threadIdx.x));
+    c = warp_sum(c);
+    if (threadIdx.x == 0) {
+      zero_amp_state x = *st;
+      amp_decide(x, c.value(), p, __ldcg(&head->beta_pow[0]), __ldcg(&head->beta_pow[1]));
+      *st = x;
+      head->arrived = 0;
+      AmpBcast b = {};
+      b.overflow = x.overflow;
+      b.coef = x.coef;
+      for (int k = 0; k < 8; ++k) b.sc[k] = x.sc[k];
+      rec = b;
+    }
   }
   __syncthreads();
   // the decision record to its kAmpCopies places, one thread each
-  if (threadIdx.x < kAmpCopies) bcast[threadIdx.x] = rec;
+  if (threadIdx.x < kAmpCopies) head->bcast[threadIdx.x] = rec;
 }
 
 __global__ void k_amp_init(zero_amp_state* st, const zero_amp_state v) { *st = v; }
 
-int launch_amp_finalize(const double* partials, int64_t n_tiles, zero_amp_state* state,
-                        AmpBcast* bcast, const AmpParams& p, void* stream) {
-  k_amp_finalize<<<1, kFinalizeThreads, 0, static_cast<cudaStream_t>(stream)>>>(partials, n_tiles,
-                                                                               state, bcast, p);
+int launch_amp_finalize(const NormPartial* partials, int64_t n_tiles, zero_amp_state* state,
+                        AmpHead* head, const AmpParams& p, void* stream) {
+  k_amp_finalize<<<kFinCtas, kFinThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      partials, n_tiles, state, head, p);
   return static_cast<int>(cudaGetLastError());
 }
 

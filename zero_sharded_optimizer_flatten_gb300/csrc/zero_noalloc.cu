@@ -11,11 +11,12 @@
 
 namespace {
 
-// The library's own scratch for zero_step_amp_noalloc: 1 MiB, which holds the
-// 4 KB of decision-record copies plus 130,560 per-tile partial sums (groups
-// of up to 267,386,880 owned elements per step).  It exists once on every
-// GPU that loads the library and stays there until the process exits.
-constexpr int64_t kNoAllocScratchBytes = INT64_C(1) << 20;
+// The library's own scratch for zero_step_amp_noalloc: 2 MiB, which holds the
+// 8 KB workspace head (decision-record copies, the decision kernel's sums)
+// plus 130,560 per-tile sums of squares of 16 bytes each (groups of up to
+// 267,386,880 owned elements per step).  It exists once on every GPU that
+// loads the library and stays there until the process exits.
+constexpr int64_t kNoAllocScratchBytes = INT64_C(2) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -66,13 +67,15 @@ extern "C" zero_status zero_step_amp_noalloc(const zero_plan* plan, const void* 
                       "scratch holds %" PRId64 " (at most %" PRId64 " tiles of 2048 elements); "
                       "use zero_step_amp with a caller-allocated workspace",
                       fn, need, kNoAllocScratchBytes,
-                      (kNoAllocScratchBytes - zero::kAmpBcastBytes) / static_cast<int64_t>(sizeof(double)));
+                      (kNoAllocScratchBytes - zero::kAmpHeadBytes) /
+                          static_cast<int64_t>(sizeof(zero::NormPartial)));
   void* scratch = nullptr;
   st = scratch_on_current_device(fn, &scratch);
   if (st != ZERO_OK) return st;
   // Every byte of the scratch that this step reads is written earlier in the
-  // same step (each tile's partial sum by the reduction, the decision record
-  // by the decision kernel), so nothing has to be cleared between calls.
+  // same step (each tile's partial sum, the beta powers and the arrival
+  // counter by the reduction; the per-CTA sums and the decision record by the
+  // decision kernel), so nothing has to be cleared between calls.
   return zero_step_amp(plan, grads, dtype, op, grad_shards, master, m, v, full_flat16,
                        out16_shard, hp, cfg, d_state, scratch, kNoAllocScratchBytes, rank_mask,
                        bucket_elems, stream);

@@ -530,7 +530,7 @@ def zero_step_amp_noalloc(plan: Plan, grads, op, grad_shards, master, m, v, full
                           out16_shard, hparams: AdamW, cfg: AmpConfig, d_state, rank_mask=None,
                           bucket_elems=0, stream=None, dtype=None):
     """zero_step_amp for callers that cannot allocate device memory: the
-    scratch is the library's fixed 1 MiB device array (steps of up to
+    scratch is the library's fixed 2 MiB device array (steps of up to
     130,560 tiles of 2048 elements).  The first call on a device sets the
     array up (make it before any stream capture); calls that overlap on the
     GPU share the array and must be serialised by the caller."""
