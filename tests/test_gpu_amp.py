@@ -220,6 +220,29 @@ def test_amp_ranks_that_own_nothing_still_decide():
     assert s.scale == 8.0
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_amp_random_groups(seed):
+    """Seeded random groups (the fused-step fuzz's draws: sizes, N up to 64,
+    modes, formats, masks, buckets) under random controls: initial scales
+    up to 2^24 (fp16 gradients then overflow until the scale has fallen),
+    windows, tolerances and clip thresholds; five calls each."""
+    from tests.test_gpu_fuzz import draw_case
+    w, bucket, _, _ = draw_case(100 + seed)
+    rng = np.random.default_rng(9000 + seed)
+    cfg = Z.AmpConfig(init_scale=float(rng.choice([1.0, 2.0 ** 8, 2.0 ** 16, 2.0 ** 24])),
+                      min_scale=1.0, window=int(rng.choice([0, 1, 2, 1000])),
+                      hysteresis=int(rng.choice([1, 2, 3])),
+                      max_norm=float(rng.choice([0.0, 1e-3, 0.05, 10.0])))
+    c = AmpCase(w, cfg, bucket=bucket)
+    for t in range(1, 6):
+        g = c.grads_scaled(t, c.ost.scale)
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        c.compare_state(f"seed {seed} call {t}")
+        c.compare(f"seed {seed} call {t}")
+
+
 def test_amp_workspace_too_small_is_rejected():
     w = W.small((30000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = AmpCase(w, Z.AmpConfig(), with_oracle=False)

@@ -1,0 +1,112 @@
+"""Seeded random parameter groups through the fused step, compared with the
+oracle over whole buffers.
+
+Each case draws a tensor-size mix (empty tensors, a few elements, sizes that
+straddle the 2048-element tiles, up to 150k), the number of virtual ranks
+(1 to 64, the compile-time paths 1..8 and the generic one), the partition
+mode and alignment, the 16-bit format, sum or average, a random rank mask,
+a bucket size, whether the ZeRO-3 shard outputs are written, and one of a
+few AdamW settings.  Two steps each; the bar is the usual one (fp32 state
+within 1e-6 relative, 16-bit parameters within 1 ulp) plus the shard
+outputs bit-identical to the oracle's.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._harness import (Case, assert_16_close, dt_code, hp_oracle, mode_code, op_code,
+                            u16)
+from zero_sharded_optimizer_flatten_gb300 import workloads as W
+from zero_sharded_optimizer_flatten_gb300 import zero as Z
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 40
+HPS = [Z.AdamW(), Z.AdamW(lr=3e-2, beta1=0.8, beta2=0.95, eps=1e-6, weight_decay=0.1),
+       Z.AdamW(lr=1e-4, weight_decay=0.0)]
+
+
+@pytest.fixture(autouse=True)
+def _cuda_cleanup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def draw_case(seed: int):
+    rng = np.random.default_rng(5000 + seed)
+    n = int(rng.integers(1, 13))
+    numel = []
+    for kind in rng.choice(5, size=n, p=[0.08, 0.2, 0.3, 0.35, 0.07]):
+        lo, hi = [(0, 1), (1, 8), (8, 301), (301, 20001), (20001, 150001)][kind]
+        numel.append(int(rng.integers(lo, hi)))
+    if sum(numel) == 0:
+        numel[0] = 1
+    N = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 12, 16, 33, 64],
+                       p=[.06, .12, .1, .12, .08, .08, .14, .06, .06, .08, .05, .05]))
+    mode = "flat" if rng.random() < 0.7 else "round_robin"
+    align = int(rng.choice([1, 2, 4, 8, 16, 32, 128])) if mode == "flat" else 1
+    dtype = "fp16" if rng.random() < 0.5 else "bf16"
+    op = "avg" if rng.random() < 0.6 else "sum"
+    bits = rng.random(N) < 0.7
+    if not bits.any():
+        bits[int(rng.integers(N))] = True
+    mask = sum(1 << r for r in range(N) if bits[r])
+    phi = sum(numel)
+    # at most about 40 buckets (each bucket is at least one launch)
+    bucket = 0 if rng.random() < 0.6 else int(rng.integers(max(1, phi // 40), 2 * phi + 2))
+    shard_out = bool(rng.random() < 0.4)
+    hp = HPS[int(rng.integers(len(HPS)))]
+    w = W.small(tuple(numel), N, mode=mode, align=align, dtype=dtype, op=op,
+                outlier_frac=0.01, seed=seed, rank_mask=mask if mask != (1 << N) - 1 else None)
+    return w, bucket, shard_out, hp
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_group_matches_oracle(seed):
+    w, bucket, shard_out, hp = draw_case(seed)
+    what = (f"seed {seed}: numel {w.numel} N={w.n_ranks} {w.mode} A={w.align} {w.dtype} "
+            f"{w.op} mask={w.mask:#x} bucket={bucket} shards={shard_out}")
+    c = Case(w)
+    S = [c.plan.shard_len(r) if (w.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+    s16 = [torch.full((n,), 0x7777, dtype=torch.int16, device="cuda").view(w.torch_dtype)
+           for n in S] if shard_out else None
+    o16 = [np.zeros(n, np.uint16) for n in S] if shard_out else None
+    for t in (1, 2):
+        g = c.grads(t)
+        Z.zero_step(c.plan, g, w.op, c.master, c.m, c.v, c.full16, s16, hp, t,
+                    rank_mask=w.mask, bucket_elems=bucket)
+        oracle.step(list(w.numel), w.n_ranks, mode_code(w), w.align, dt_code(w), op_code(w),
+                    [u16(x) for x in g], c.o_master, c.o_m, c.o_v, c.o_full, o16,
+                    hp_oracle(hp), t, w.mask)
+    torch.cuda.synchronize()
+    c.compare(what)
+    if shard_out:
+        for r in range(w.n_ranks):
+            if S[r]:
+                assert_16_close(u16(s16[r]), o16[r], f"{what} shard16[{r}]",
+                                dtype_code=dt_code(w))
+    # the plan the library built is the oracle's, bit for bit
+    for r in range(w.n_ranks):
+        seg = oracle.segments(list(w.numel), w.n_ranks, mode_code(w), w.align, r)
+        assert np.array_equal(c.plan.segments(r), seg), what
+
+
+def test_fuzz_covers_the_dispatch_paths():
+    """The drawn cases reach every kind of launch the step has."""
+    draws = [draw_case(s) for s in range(N_CASES)]
+    Ns = {w.n_ranks for w, *_ in draws}
+    assert Ns & {1, 2, 3, 4, 5, 7, 8} and Ns & {9, 12, 16, 33, 64}
+    assert {w.mode for w, *_ in draws} == {"flat", "round_robin"}
+    assert {w.dtype for w, *_ in draws} == {"fp16", "bf16"}
+    assert {w.op for w, *_ in draws} == {"sum", "avg"}
+    assert any(b for _, b, _, _ in draws) and any(not b for _, b, _, _ in draws)
+    assert any(s for _, _, s, _ in draws)
+    assert any(w.rank_mask is not None for w, *_ in draws)
+    assert any(0 in w.numel for w, *_ in draws)
