@@ -238,12 +238,39 @@ def oracle_rate(w, n_elems: int):
     return n_elems / el, el
 
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: its logical CPU count and model name."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "processor name") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:  # Arm hosts list no model name in /proc/cpuinfo
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "model": model}
+
+
 def cpu_baseline(w, budget_s: float = 10.0):
     rate, _ = oracle_rate(w, 1 << 16)
     n = int(min(w.phi, max(1 << 16, rate * budget_s)))
     n -= n % 8
     rate, el = oracle_rate(w, n)
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": f"{n} elements of the {w.key} group (all {w.n_ranks} gradient replicas), "
                       f"one step of the single-threaded C oracle, {el:.1f} s"}
 
@@ -281,6 +308,7 @@ def run_reference(args, world, rank):
         "config": {"workload": w.title, "phi": w.phi,
                    "virtual_ranks": w.n_ranks, "sample_elements_per_step": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"{n} of {w.phi} elements per step, single-threaded C oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -764,18 +792,20 @@ def run_unfused(args, world, rank, local):
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
-    S = [plan.shard_len(r) for r in range(w.n_ranks)]
-    p16 = W.params16(w, dev)
+    mask, bucket = w.mask, w.bucket_elems
+    S = [plan.shard_len(r) if (mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+    ext = plan.flat_extent(mask)
+    p16 = W.fill(w, "param", 0, 0, 0, ext, torch.empty(ext, dtype=w.torch_dtype, device=dev))
     full = torch.zeros_like(p16)
     master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
     m = [torch.empty_like(x) for x in master]
     v = [torch.empty_like(x) for x in master]
-    Z.zero_init_shards(plan, p16, master, m, v)
+    Z.zero_init_shards(plan, p16, master, m, v, rank_mask=mask)
     gsh = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
     s16 = [torch.empty(n, dtype=w.torch_dtype, device=dev) for n in S]
-    grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+    grads = [W.grads16(w, 1, q, dev, 0, ext) for q in range(w.n_ranks)]
     hp = Z.AdamW()
-    E = plan.padded
+    E = sum(S)          # elements of the masked shards
     per = {"k_reduce_scatter": 2 * w.n_ranks + 4, "k_adamw": 30, "k_allgather": 4}
 
     def pair():
@@ -788,15 +818,15 @@ def run_unfused(args, world, rank, local):
         i = k - args.warmup
         if rec:
             ev["k_reduce_scatter"][i][0].record()
-        Z.zero_reduce_scatter(plan, grads, w.op, gsh)
+        Z.zero_reduce_scatter(plan, grads, w.op, gsh, rank_mask=mask, bucket_elems=bucket)
         if rec:
             ev["k_reduce_scatter"][i][1].record()
             ev["k_adamw"][i][0].record()
-        Z.zero_adamw_shard_step(plan, master, m, v, gsh, s16, hp, t)
+        Z.zero_adamw_shard_step(plan, master, m, v, gsh, s16, hp, t, rank_mask=mask)
         if rec:
             ev["k_adamw"][i][1].record()
             ev["k_allgather"][i][0].record()
-        Z.zero_allgather(plan, s16, full)
+        Z.zero_allgather(plan, s16, full, rank_mask=mask)
         if rec:
             ev["k_allgather"][i][1].record()
     torch.cuda.synchronize(dev)
@@ -808,14 +838,69 @@ def run_unfused(args, world, rank, local):
         total += sec
         kernels[k] = {"us": 1e6 * sec, "bytes": b * E, "GB/s": b * E / sec / 1e9,
                       "frac": b * E / sec / 1e9 / peak}
-    line = {"impl": "gb300", "metric": METRIC, "value": plan.phi / total, "unit": UNIT,
+    line = {"impl": "gb300", "metric": METRIC, "value": E / total, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.title, "phi": plan.phi,
+            "config": {"workload": w.title, "phi": plan.phi, "elements_per_step": E,
                        "path": "unfused: reduce-scatter, AdamW + cast, all-gather",
                        "kernels": kernels,
                        "bytes_per_element": sum(per.values())}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gather_all(args, world, rank, local):
+    """zero_allgather of every rank's 16-bit shard into the whole flat buffer
+    (the all-gather row at full size; for the LLaMA-7B group 6.74 G elements,
+    4 B each: 26.95 GB per call).  Flat groups only: the shards are views of
+    one flat parameter buffer, and the gathered buffer must equal it."""
+    import torch
+
+    import zero_sharded_optimizer_flatten_gb300 as Z
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    if w.mode != "flat":
+        raise SystemExit("--gather-all: flat groups only")
+    plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
+    src = W.params16(w, dev)
+    shards = [src[off:off + n] for off, n in plan.shards]
+    full = torch.zeros_like(src)
+    E = plan.padded
+    for _ in range(args.warmup):
+        Z.zero_allgather(plan, shards, full)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    for a, b in ev:
+        a.record()
+        Z.zero_allgather(plan, shards, full)
+        b.record()
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clocks.stop()
+    assert torch.equal(full, src), "the gathered buffer differs from the shards' source"
+    sec = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
+    peak, peak_src = measured_peaks()
+    gbs = 4 * E / sec / 1e9
+    line = {"impl": "gb300", "metric": METRIC, "value": E / sec, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": w.title + ": all-gather of every rank's shard",
+                       "elements_per_call": E, "bytes_per_call": 4 * E,
+                       "l2": f"inputs larger than L2: {4 * E / 1e6:.1f} MB per call"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "kernel": "k_allgather",
+                         "bytes_per_launch": 4 * E, "peak_source": peak_src},
+            "gpu_launches": args.steps, "clocks": clocks.summary(t0, t1)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -913,6 +998,9 @@ def main(argv=None):
                          "steps captured in one CUDA graph (the default for flat groups)")
     ap.add_argument("--unfused", action="store_true",
                     help="time the three unfused calls of a step separately")
+    ap.add_argument("--gather-all", action="store_true",
+                    help="time the all-gather of every rank's shard into the whole flat "
+                         "buffer (flat groups)")
     ap.add_argument("--offload-cpu", action="store_true",
                     help="ZeRO-Offload with the CPU optimizer (host threads run AdamW)")
     ap.add_argument("--threads", type=int, default=0,
@@ -937,6 +1025,8 @@ def main(argv=None):
         return run_offload_cpu(args, world, rank, local)
     if args.unfused:
         return run_unfused(args, world, rank, local)
+    if args.gather_all:
+        return run_gather_all(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 

@@ -44,6 +44,15 @@ constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 #ifndef ZERO_GRID_MULT
 #define ZERO_GRID_MULT 0
 #endif
+// Consecutive 2048-element tiles one CTA of the all-gather copies.  Measured
+// (zero_allgather of every shard): LLaMA-7B group 6421 / 7199 / 7156 / 7167
+// GB/s for 1 / 2 / 4 / 8 tiles, BERT-base 5919 / 6783 / 6600 / 6640, one
+// LLaMA-13B MLP layer 6250 / 6975 / 6841 / 6841.
+#ifndef ZERO_GATHER_TILES
+#define ZERO_GATHER_TILES 2
+#endif
+constexpr int kGatherTiles = ZERO_GATHER_TILES;
+
 // Bounds-checked build: every kernel access is checked against the plan's
 // buffer lengths; a violation skips the access and sets the device error
 // word to 2 (zero_sync reports it).

@@ -383,23 +383,58 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw(const __gri
       });
 }
 
-// All-gather: copy each rank's 16-bit shard into the flat buffer.
+// All-gather: copy each rank's 16-bit shard into the flat buffer.  A copy
+// moves only 8 KB per 2048-element tile, too little to amortise a CTA, so a
+// CTA copies kGatherTiles consecutive tiles and issues every load before the
+// first store.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_allgather(const __grid_constant__ LaunchArgs a) {
-  for_each_tile(
-      a,
-      [&](const Job& jb, int64_t e0, bool two) {
-        const uint16_t* src = static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e0;
+  constexpr int K = kGatherTiles;
+  const uint2 z = make_uint2(0u, 0u);
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * K; t0 < a.n_tiles;
+       t0 += static_cast<int64_t>(gridDim.x) * K) {
+    int job[K];
+    uint2 w[K][2];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t tile = t0 + k;
+      job[k] = tile < a.n_tiles ? find_job(a, tile) : -1;
+      w[k][0] = w[k][1] = z;
+      if (job[k] < 0) continue;
+      const Job& jb = a.jobs[job[k]];
+      const int64_t e0 = (tile - jb.tile_begin) * kTile + static_cast<int64_t>(threadIdx.x) * kVec;
+      if (!jb.vec || e0 >= jb.len) continue;
+      const bool two = e0 + kHalf < jb.len;
+      if (!access_ok(a, jb, e0, kVec) || (two && !access_ok(a, jb, e0 + kHalf, kVec))) continue;
+      const uint16_t* src = static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e0;
+      w[k][0] = ld_once8(src);
+      if (two) w[k][1] = ld_once8(src + kHalf);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (job[k] < 0) continue;
+      const int64_t tile = t0 + k;
+      const Job& jb = a.jobs[job[k]];
+      const int64_t base = (tile - jb.tile_begin) * kTile;
+      if (jb.vec) {
+        const int64_t e0 = base + static_cast<int64_t>(threadIdx.x) * kVec;
+        if (e0 >= jb.len) continue;
+        const bool two = e0 + kHalf < jb.len;
+        if (!access_ok(a, jb, e0, kVec) || (two && !access_ok(a, jb, e0 + kHalf, kVec))) continue;
         uint16_t* dst = static_cast<uint16_t*>(a.full16) + jb.flat_off + e0;
-        const uint2 w0 = ld_once8(src);
-        const uint2 w1 = two ? ld_once8(src + kHalf) : make_uint2(0u, 0u);
-        st_quad16(dst, w0);
-        if (two) st_quad16(dst + kHalf, w1);
-      },
-      [&](const Job& jb, int64_t e) {
-        static_cast<uint16_t*>(a.full16)[jb.flat_off + e] =
-            ld_once16(static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e);
-      });
+        st_quad16(dst, w[k][0]);
+        if (two) st_quad16(dst + kHalf, w[k][1]);
+      } else {
+#pragma unroll 1
+        for (int i = 0; i < kTile / kThreads; ++i) {
+          const int64_t e = base + i * kThreads + threadIdx.x;
+          if (e < jb.len && access_ok(a, jb, e, 1))
+            static_cast<uint16_t*>(a.full16)[jb.flat_off + e] =
+                ld_once16(static_cast<const uint16_t*>(a.shard16[jb.rank]) + jb.shard_off + e);
+        }
+      }
+    }
+  }
 }
 
 // Initialise a rank's fp32 master from its 16-bit partition; zero m and v.
@@ -730,7 +765,9 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kStats: fn = by_ranks<T, PickStats>(a.n_ranks); break;
     case Kind::kAdamwAmp: fn = reinterpret_cast<const void*>(&k_adamw_amp<T>); break;
   }
-  int grid = grid_for(fn, a.n_tiles);
+  const int64_t units = kind == Kind::kAllgather ? (a.n_tiles + kGatherTiles - 1) / kGatherTiles
+                                                 : a.n_tiles;
+  int grid = grid_for(fn, units);
   if (kind == Kind::kStats && grid == 0) grid = 1;  // an empty launch still prepares the decision
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
