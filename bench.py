@@ -232,6 +232,27 @@ class OracleSample:
                                     self.hp, t, out16=self.out)
         return time.perf_counter() - t0
 
+    def step_threads(self, t: int, k: int) -> float:
+        """The same oracle call over k contiguous element ranges on k host
+        threads (the C oracle runs with the interpreter lock released); the
+        per-thread copies of the gradient columns are made before timing."""
+        import concurrent.futures as cf
+
+        import numpy as np
+        if getattr(self, "_parts_k", None) != k:
+            cut = [min(self.n, (self.n * i // k) // 8 * 8) for i in range(k)] + [self.n]
+            self._parts = [(np.ascontiguousarray(self.grads[:, a:b]), a, b)
+                           for a, b in zip(cut[:-1], cut[1:]) if b > a]
+            self._parts_k = k
+        with cf.ThreadPoolExecutor(len(self._parts)) as pool:
+            t0 = time.perf_counter()
+            futs = [pool.submit(self.oracle.update_elements, g, self.master[a:b], self.m[a:b],
+                                self.v[a:b], self.dt, self.op, self.hp, t, self.out[a:b])
+                    for g, a, b in self._parts]
+            for f in futs:
+                f.result()
+            return time.perf_counter() - t0
+
 
 def oracle_rate(w, n_elems: int):
     el = OracleSample(w, n_elems).step(1)
@@ -269,10 +290,21 @@ def cpu_baseline(w, budget_s: float = 10.0):
     rate, _ = oracle_rate(w, 1 << 16)
     n = int(min(w.phi, max(1 << 16, rate * budget_s)))
     n -= n % 8
-    rate, el = oracle_rate(w, n)
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
-            "sample": f"{n} elements of the {w.key} group (all {w.n_ranks} gradient replicas), "
-                      f"one step of the single-threaded C oracle, {el:.1f} s"}
+    sample = OracleSample(w, n)
+    el = sample.step(1)
+    out = {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
+           "sample": f"{n} elements of the {w.key} group (all {w.n_ranks} gradient replicas), "
+                     f"one step of the single-threaded C oracle, {el:.1f} s"}
+    # the same plain oracle over all host cores (element ranges split evenly)
+    k = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+            else os.cpu_count() or 1)
+    if k > 1:
+        sample.step_threads(2, k)                       # warm the pool's threads
+        el_k = min(sample.step_threads(3 + i, k) for i in range(2))
+        out["all_cores"] = {"value": n / el_k, "unit": UNIT, "cores": k, "kind": "oracle",
+                            "sample": f"the same {n} elements split over {k} host threads, "
+                                      f"best of 2 steps, {el_k:.2f} s"}
+    return out
 
 
 # ----------------------------------------------------------------------------
