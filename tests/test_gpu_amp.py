@@ -243,6 +243,24 @@ def test_amp_random_groups(seed):
         c.compare(f"seed {seed} call {t}")
 
 
+def test_amp_many_tensors_number_tiles_across_launches():
+    """700 round-robin tensors: the reduction needs several launches per call
+    and each numbers its tiles after the previous ones (the per-tile sums
+    must land in distinct workspace slots)."""
+    rng = np.random.default_rng(3)
+    numel = tuple(int(x) for x in rng.integers(1, 3000, size=700))
+    w = W.small(numel, 3, mode="round_robin", align=1, dtype="fp16", op="sum",
+                outlier_frac=0.01)
+    c = AmpCase(w, Z.AmpConfig(init_scale=256.0, window=2, hysteresis=1, max_norm=0.05))
+    for t in range(1, 4):
+        g = c.grads_scaled(t, c.ost.scale)
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        c.compare_state(f"many tensors call {t}")
+        c.compare(f"many tensors call {t}")
+
+
 def test_amp_workspace_too_small_is_rejected():
     w = W.small((30000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = AmpCase(w, Z.AmpConfig(), with_oracle=False)

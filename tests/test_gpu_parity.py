@@ -87,6 +87,36 @@ def test_other_hyperparameters(hp):
     _run_full(w, 4, hp=hp)
 
 
+def _many_tensors(n=700, seed=3):
+    rng = np.random.default_rng(seed)
+    return tuple(int(x) for x in rng.integers(1, 3000, size=n))
+
+
+def test_many_tensors_need_several_launches():
+    """700 round-robin tensors of odd sizes over 3 ranks: every tensor is its
+    own run, most split into head, quad body and tail jobs, so one call needs
+    far more than the 192 jobs one launch carries; whole buffers and the
+    16-bit shard outputs are compared with the oracle."""
+    numel = _many_tensors()
+    w = W.small(numel, 3, mode="round_robin", align=1, dtype="fp16", op="sum")
+    plan = Z.zero_plan_partitions(list(numel), 3, "round_robin", 1)
+    runs = sum(len(plan.segments(r)) for r in range(3))
+    assert runs >= 700
+    before = Z.zero_launch_count()
+    c = _run_full(w, 2)
+    assert Z.zero_launch_count() - before >= 2 * (runs // 192 + 1)
+    s16 = [torch.empty(c.plan.shard_len(r), dtype=w.torch_dtype, device="cuda") for r in range(3)]
+    g = c.grads(3)
+    Z.zero_step(c.plan, g, "sum", c.master, c.m, c.v, c.full16, s16, HP, 3)
+    o16 = [np.zeros(c.plan.shard_len(r), np.uint16) for r in range(3)]
+    oracle.step(list(numel), 3, oracle.ROUND_ROBIN, 1, dt_code(w), oracle.SUM,
+                [u16(x) for x in g], c.o_master, c.o_m, c.o_v, c.o_full, o16, hp_oracle(HP), 3)
+    torch.cuda.synchronize()
+    c.compare("many tensors step 3")
+    for r in range(3):
+        assert np.array_equal(u16(s16[r]), o16[r])
+
+
 def test_large_step_count():
     """Bias-correction constants at t = 1000 (beta2^t far from 1)."""
     w = W.small((4096, 100), 2, mode="flat", align=16, dtype="fp16", op="avg")
