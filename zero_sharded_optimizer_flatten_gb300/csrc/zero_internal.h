@@ -53,6 +53,15 @@ constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 #endif
 constexpr int kGatherTiles = ZERO_GATHER_TILES;
 
+// Programmatic dependent launch (tuning switch): every kernel is launched
+// with the programmatic-stream-serialization attribute, waits for the grid
+// before it (griddepcontrol.wait) before touching global memory, and then
+// lets the grid after it launch (griddepcontrol.launch_dependents), so a
+// launch overlaps the tail of its predecessor instead of following it.
+#ifndef ZERO_PDL
+#define ZERO_PDL 0
+#endif
+
 // Bounds-checked build: every kernel access is checked against the plan's
 // buffer lengths; a violation skips the access and sets the device error
 // word to 2 (zero_sync reports it).

@@ -240,6 +240,41 @@ __device__ __forceinline__ void store_16x2(void* base, int64_t i0, int64_t i1, b
 }
 
 // ---------------------------------------------------------------------------
+// launch ordering
+
+// First statement of every kernel: with ZERO_PDL, wait until the preceding
+// grid on the stream has completed and its writes are visible, then allow
+// the next grid to launch.  Without it (or without the launch attribute)
+// stream order alone separates the kernels.
+__device__ __forceinline__ void grid_dependency_begin() {
+#if ZERO_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+// Host: launch `fn` on `s`, with the programmatic-serialization attribute
+// when ZERO_PDL is set.
+inline cudaError_t launch_ordered(const void* fn, dim3 grid, dim3 block, void** args,
+                                  size_t smem, cudaStream_t s) {
+#if ZERO_PDL
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+#else
+  return cudaLaunchKernel(fn, grid, block, args, smem, s);
+#endif
+}
+
+// ---------------------------------------------------------------------------
 // tile -> job
 
 __device__ __forceinline__ int find_job(const LaunchArgs& a, int64_t tile) {
@@ -301,6 +336,7 @@ __device__ __forceinline__ void for_each_tile(const LaunchArgs& a, BodyVec body_
 // Fused step: reduce-scatter + AdamW + cast + all-gather.
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_step(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   for_each_tile(
       a,
       [&](const Job& jb, int64_t e0, bool two) {
@@ -338,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_step(const __grid
 // Reduce-scatter alone: fp32 gradient shards.
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_reduce_scatter(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   for_each_tile(
       a,
       [&](const Job& jb, int64_t e0, bool two) {
@@ -354,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_reduce_scatter(co
 // AdamW + cast on fp32 gradient shards.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   for_each_tile(
       a,
       [&](const Job& jb, int64_t e0, bool two) {
@@ -389,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw(const __gri
 // first store.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_allgather(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   constexpr int K = kGatherTiles;
   const uint2 z = make_uint2(0u, 0u);
   for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * K; t0 < a.n_tiles;
@@ -440,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_allgather(const _
 // Initialise a rank's fp32 master from its 16-bit partition; zero m and v.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_init(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   for_each_tile(
       a,
       [&](const Job& jb, int64_t e0, bool two) {
@@ -599,6 +639,7 @@ __device__ __forceinline__ void tile_sum_barrier(SqSum s, SqSum* warp_part, Norm
 // tiles, the block-wide barrier version is used.
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   __shared__ SqSum warp_part[kThreads / 32];
   __shared__ int arrived;
   const bool one_tile = static_cast<int64_t>(gridDim.x) >= a.n_tiles;
@@ -655,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
 // kernel's coefficient; does nothing when the decision was to skip.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw_amp(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   __shared__ uint4 rec[sizeof(AmpBcast) / 16];
   if (threadIdx.x < sizeof(AmpBcast) / 16)
     rec[threadIdx.x] = __ldcg(reinterpret_cast<const uint4*>(a.bcast + blockIdx.x % kAmpCopies) +
@@ -771,7 +813,7 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
   if (kind == Kind::kStats && grid == 0) grid = 1;  // an empty launch still prepares the decision
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
-  return static_cast<int>(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, s));
+  return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args, 0, s));
 }
 
 }  // namespace zero

@@ -89,6 +89,7 @@ constexpr int tma_stage_bytes() {
 
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, 1) k_step_tma(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) unsigned long long full_bar[kTmaStages];
   __shared__ int ok;
@@ -242,7 +243,7 @@ int launch_step_tma_impl(const LaunchArgs& a, cudaStream_t s) {
   const int grid = tma_grid(fn, smem, a.n_tiles);
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
-  return static_cast<int>(cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args,
+  return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args,
                                            static_cast<size_t>(smem), s));
 }
 

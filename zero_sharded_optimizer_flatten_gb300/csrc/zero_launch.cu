@@ -94,6 +94,7 @@ __device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p, 
 __global__ void __launch_bounds__(kFinThreads) k_amp_finalize(const NormPartial* partials,
                                                               int64_t n, zero_amp_state* st,
                                                               AmpHead* head, const AmpParams p) {
+  grid_dependency_begin();
   constexpr int64_t kAll = static_cast<int64_t>(kFinCtas) * kFinThreads;
   const float4* src = reinterpret_cast<const float4*>(partials);
   SqSum s = sq_zero();
@@ -147,9 +148,11 @@ __global__ void k_amp_init(zero_amp_state* st, const zero_amp_state v) { *st = v
 
 int launch_amp_finalize(const NormPartial* partials, int64_t n_tiles, zero_amp_state* state,
                         AmpHead* head, const AmpParams& p, void* stream) {
-  k_amp_finalize<<<kFinCtas, kFinThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      partials, n_tiles, state, head, p);
-  return static_cast<int>(cudaGetLastError());
+  AmpParams params = p;
+  void* args[] = {const_cast<NormPartial**>(&partials), &n_tiles, &state, &head, &params};
+  return static_cast<int>(launch_ordered(reinterpret_cast<const void*>(&k_amp_finalize),
+                                         dim3(kFinCtas), dim3(kFinThreads), args, 0,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream) {
