@@ -41,7 +41,8 @@
  *  - At most 64 virtual ranks; rank_mask bit r selects rank r.  Pointer
  *    arrays are indexed by rank and have n_ranks entries; entries of ranks
  *    outside rank_mask, or whose shard is empty, are not read and may be
- *    NULL.
+ *    NULL.  Likewise any buffer of zero length (a group whose tensors are
+ *    all empty has an empty flat buffer) may be NULL.
  *  - Flat indices f run over the gathered flat buffer (length `padded` from
  *    zero_plan_total); shard indices i run over rank r's shard buffers
  *    (length from zero_plan_shard).

@@ -261,6 +261,20 @@ def test_amp_many_tensors_number_tiles_across_launches():
         c.compare(f"many tensors call {t}")
 
 
+def test_amp_group_without_elements_still_decides():
+    """Every tensor empty: the norm is 0, the step counts, the scale grows
+    after its window, exactly as the oracle's state machine says."""
+    w = W.small((0, 0), 2, mode="flat", align=16, dtype="fp16", op="avg")
+    c = AmpCase(w, Z.AmpConfig(init_scale=8.0, window=1, hysteresis=1))
+    for t in (1, 2):
+        g = [torch.empty(0, dtype=torch.float16, device="cuda") for _ in range(2)]
+        c.gpu_step(g)
+        c.oracle_step_amp(g)
+        torch.cuda.synchronize()
+        s = c.compare_state(f"empty group call {t}")
+        assert s.step == t and s.norm == 0.0 and s.scale == 8.0 * 2 ** t
+
+
 def test_amp_workspace_too_small_is_rejected():
     w = W.small((30000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = AmpCase(w, Z.AmpConfig(), with_oracle=False)

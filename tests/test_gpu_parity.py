@@ -71,6 +71,7 @@ SMALL = [
     ((70001,), 7, "flat", 1, "fp16", "sum"),                             # one ragged tensor
     ((1,), 4, "flat", 16, "bf16", "avg"),                                # one element
     ((5, 3), 2, "round_robin", 1, "fp16", "avg"),
+    ((1000, 37), 64, "flat", 4096, "bf16", "avg"),                       # largest A: 262,144
 ]
 
 
@@ -115,6 +116,22 @@ def test_many_tensors_need_several_launches():
     c.compare("many tensors step 3")
     for r in range(3):
         assert np.array_equal(u16(s16[r]), o16[r])
+
+
+@pytest.mark.parametrize("mode", ["flat", "round_robin"])
+def test_groups_without_elements(mode):
+    """Every tensor empty: the plan has no element, a step launches nothing
+    and succeeds, and the oracle agrees that nothing changes."""
+    numel = (0, 0, 0)
+    plan = Z.zero_plan_partitions(list(numel), 4, mode, 16)
+    assert (plan.phi, plan.padded) == (0, 0)
+    assert all(plan.shard_len(r) == 0 for r in range(4))
+    empty16 = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    empty32 = [torch.empty(0, dtype=torch.float32, device="cuda") for _ in range(4)]
+    before = Z.zero_launch_count()
+    Z.zero_step(plan, [empty16] * 4, "avg", empty32, empty32, empty32, empty16, None, HP, 1)
+    Z.zero_sync()
+    assert Z.zero_launch_count() == before
 
 
 def test_large_step_count():

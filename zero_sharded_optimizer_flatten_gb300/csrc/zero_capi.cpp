@@ -64,7 +64,9 @@ zero_status check_dtype(const char* fn, zero_dtype dtype) {
 }
 
 // Per-rank pointer array: every masked rank's entry non-NULL (unless
-// nullable) and 16-byte aligned.
+// nullable) and 16-byte aligned.  all_ranks: the entries are the flat
+// gradient replicas, which every rank must supply unless the flat buffer is
+// empty.
 template <class P>
 zero_status check_ptrs(const char* fn, const char* what, P const* arr, const zero_plan* plan,
                        uint64_t mask, bool nullable_entries, bool all_ranks = false) {
@@ -72,6 +74,7 @@ zero_status check_ptrs(const char* fn, const char* what, P const* arr, const zer
   for (int r = 0; r < plan->n_ranks; ++r) {
     if (!all_ranks && !in_mask(mask, r)) continue;
     if (!all_ranks && plan->shard_len[r] == 0) continue;  // an empty shard is never touched
+    if (all_ranks && plan->padded == 0) continue;          // nor is an empty flat buffer
     const void* p = arr[r];
     if (!p) {
       if (nullable_entries) continue;
@@ -252,7 +255,8 @@ extern "C" zero_status zero_init_shards(const zero_plan* plan, const void* full_
   clear_error();
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
-  if (!full_flat16) return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
+  if (!full_flat16 && plan->padded > 0)
+    return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
   if (!aligned16(full_flat16)) return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
   ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
@@ -434,7 +438,8 @@ extern "C" zero_status zero_allgather(const zero_plan* plan, const void* const* 
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
   ZERO_TRY(check_ptrs(fn, "shards16", shards16, plan, rank_mask, false));
-  if (!full_flat16) return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
+  if (!full_flat16 && plan->padded > 0)
+    return fail(ZERO_ERR_INVALID, "%s: full_flat16 is NULL", fn);
   if (!aligned16(full_flat16)) return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
   ZERO_TRY(pending_error(fn));
   ArgsHolder h(new_args());
