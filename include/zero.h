@@ -378,6 +378,26 @@ zero_status zero_step_amp(const zero_plan* plan, const void* const* grads, zero_
                           void* stream);
 
 /*
+ * The mixed-precision step from gradients that are already reduce-scattered:
+ * grad_shards[r] (read only) holds rank r's reduced, still loss-scaled fp32
+ * gradient, as zero_reduce_scatter or zero_reduce_scatter_range leave it --
+ * the flow of a training loop that reduces gradient buckets while the
+ * backward pass runs ("DeepSpeed ZeRO-2 ..." §2.2, §4.2: overlap_comm and the
+ * reduction stream) and then checks for overflow, clips and updates the
+ * partitions.  Everything else (norm, skip, loss scale, clip, AdamW, cast,
+ * gather, workspace, state) is as zero_step_amp; the workspace size is
+ * zero_amp_workspace_bytes(plan, rank_mask, bucket_elems) for the same
+ * bucket_elems.  The results equal zero_reduce_scatter followed by this call
+ * and zero_step_amp on the replicas, bit for bit.
+ */
+zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dtype,
+                                 float* const* grad_shards, float* const* master, float* const* m,
+                                 float* const* v, void* full_flat16, void* const* out16_shard,
+                                 const zero_adamw_hparams* hp, const zero_amp_config* cfg,
+                                 void* d_state, void* workspace, int64_t workspace_bytes,
+                                 uint64_t rank_mask, int64_t bucket_elems, void* stream);
+
+/*
  * zero_step_amp without a workspace argument, for callers that cannot
  * allocate device memory: code whose device memory all comes from a fixed
  * budget or pool it does not control, or that runs where a cudaMalloc /

@@ -275,6 +275,49 @@ def test_amp_group_without_elements_still_decides():
         assert s.step == t and s.norm == 0.0 and s.scale == 8.0 * 2 ** t
 
 
+@pytest.mark.parametrize("bucket,mode", [(0, "flat"), (4096, "flat"), (0, "round_robin")])
+def test_amp_from_reduced_shards_equals_the_fused_step(bucket, mode):
+    """zero_reduce_scatter then zero_step_amp_shards == zero_step_amp, bit for
+    bit, through an overflow trajectory (fp16 gradients at a scale of 2^20):
+    the same decisions, state, shards and gathered parameters."""
+    w = W.small((30000, 37, 4096, 3, 129), 4, mode=mode, align=16, dtype="fp16", op="avg",
+                outlier_frac=0.01)
+    cfg = Z.AmpConfig(init_scale=2.0 ** 20, min_scale=1.0, window=2, hysteresis=2,
+                      max_norm=0.05)
+    a = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    b = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    skipped = 0
+    for t in range(1, 9):
+        g = a.grads_scaled(t, Z.read_amp_state(a.state).scale)
+        a.gpu_step(g)
+        Z.zero_reduce_scatter(b.plan, g, "avg", b.gsh, bucket_elems=bucket)
+        Z.zero_step_amp_shards(b.plan, b.gsh, b.master, b.m, b.v, b.full16, None, HP, cfg,
+                               b.state, b.ws, bucket_elems=bucket)
+        torch.cuda.synchronize()
+        assert torch.equal(a.state, b.state), t
+        skipped = Z.read_amp_state(a.state).skipped
+        # bit patterns: overflowing steps leave NaNs in the reduced shards
+        bits = lambda x: x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16)  # noqa: E731
+        for r in range(4):
+            for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.gsh, b.gsh)):
+                assert torch.equal(bits(x[r]), bits(y[r])), (t, r)
+        assert torch.equal(bits(a.full16), bits(b.full16)), t
+    assert 0 < skipped < 8
+
+
+def test_amp_shards_rejects_bad_arguments_without_launching():
+    w = W.small((5000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
+    c = AmpCase(w, Z.AmpConfig(), with_oracle=False)
+    before = Z.zero_launch_count()
+    with pytest.raises(Z.ZeroError):
+        Z.zero_step_amp_shards(c.plan, c.gsh, c.master, c.m, c.v, c.full16, None, HP, c.cfg,
+                               c.state, c.ws[:8])
+    with pytest.raises(ValueError):
+        Z.zero_step_amp_shards(c.plan, c.gsh, c.master, c.m, c.v, None, None, HP, c.cfg,
+                               c.state, c.ws)   # no 16-bit buffer to infer the format from
+    assert Z.zero_launch_count() == before
+
+
 def test_amp_workspace_too_small_is_rejected():
     w = W.small((30000,), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = AmpCase(w, Z.AmpConfig(), with_oracle=False)

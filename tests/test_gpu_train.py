@@ -10,6 +10,10 @@ parameters rounded back to bf16 after every step.  torch's AdamW rounds its
 moment update differently (a lerp), so the two runs are compared as loss
 curves, not bit for bit; the bit-level parity of each piece is covered by the
 engine and parity tests.
+
+The second test runs the engine's mixed-precision form: an fp16 model with a
+dynamic loss scale, overflow skips and clipping, checked step by step against
+zero_step_amp on the engine's own replicas, and for convergence.
 """
 import copy
 import gc
@@ -103,4 +107,58 @@ def test_engine_trains_like_torch_adamw():
     for t in range(STEPS):
         assert abs(curve_eng[t] - curve_ref[t]) <= 2e-2 * curve_ref[t], (t, curve_eng[t],
                                                                         curve_ref[t])
+    eng.remove_hooks()
+
+
+def test_engine_mixed_precision_step_and_training():
+    """fp16 student with a dynamic loss scale starting at 2^24 (the first
+    backward passes overflow fp16 and are skipped while the scale falls),
+    clipping at 1.0.  Each iteration, the engine's step (overlapped bucket
+    reductions, then zero_step_amp_shards) must equal zero_step_amp run on
+    copies of the engine's own gradient replicas and state, bit for bit; and
+    the model must train."""
+    teacher = _mlp(123, torch.float32)
+    student = _mlp(1, torch.float16)
+    cfg = Z.AmpConfig(init_scale=2.0 ** 24, min_scale=1.0, window=20, hysteresis=1,
+                      max_norm=1.0)
+    hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    eng = ZeroEngine(student.parameters(), N, mode="flat", align=16, op="avg", hparams=hp,
+                     bucket_elems=20_000, overlap_comm=True, amp=cfg)
+    plan = eng.plan
+
+    def loss_of(model, x):
+        with torch.no_grad():
+            y = teacher(x)
+        return (model(x.to(torch.float16)).float() - y).pow(2).mean()
+
+    curve = []
+    for t in range(STEPS):
+        xs = [_micro_batch(q, t) for q in range(N)]
+        le = 0.0
+        for q in range(N):
+            loss = loss_of(student, xs[q])
+            eng.backward(loss, q)
+            le += loss.item() / N
+        curve.append(le)
+        # the same step by zero_step_amp on copies of the replicas and state
+        torch.cuda.current_stream().wait_stream(eng.reduction_stream)
+        grads = [g.clone() for g in eng.grads]
+        copies = {k: [x.clone() for x in getattr(eng, k)] for k in ("master", "m", "v")}
+        state = eng.amp_state.clone()
+        flat = eng.flat16.clone()
+        gsh = [torch.empty_like(x) for x in eng.grad_shards]
+        ws = torch.empty_like(eng._workspace)
+        Z.zero_step_amp(plan, grads, "avg", gsh, copies["master"], copies["m"], copies["v"],
+                        flat, None, hp, cfg, state, ws)
+        eng.step()
+        torch.cuda.synchronize()
+        assert torch.equal(state, eng.amp_state), t
+        assert torch.equal(flat, eng.flat16), t
+        for k in ("master", "m", "v"):
+            for r in range(N):
+                assert torch.equal(copies[k][r], getattr(eng, k)[r]), (t, k, r)
+    st = eng.amp_status()
+    assert st.skipped >= 1 and st.step == STEPS - st.skipped
+    assert st.scale < 2.0 ** 24
+    assert curve[-1] < 0.5 * curve[0], (curve[0], curve[-1])
     eng.remove_hooks()

@@ -15,4 +15,5 @@ from .zero import (AMP_STATE_BYTES, ZERO_BF16, ZERO_FP16, ZERO_PART_FLAT,  # noq
                    zero_plan_segments, zero_plan_shard, zero_plan_total, zero_reduce_scatter,
                    zero_reduce_scatter_range,
                    zero_selftest_wait_timeout, zero_step, zero_step_amp, zero_step_amp_noalloc,
+                   zero_step_amp_shards,
                    zero_sync, zero_version, zero_zero3_pass)

@@ -521,23 +521,26 @@ extern "C" zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t 
   return ZERO_OK;
 }
 
-extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* grads,
-                                     zero_dtype dtype, zero_reduce_op op,
-                                     float* const* grad_shards, float* const* master,
-                                     float* const* m, float* const* v, void* full_flat16,
-                                     void* const* out16_shard, const zero_adamw_hparams* hp,
-                                     const zero_amp_config* cfg, void* d_state, void* workspace,
-                                     int64_t workspace_bytes, uint64_t rank_mask,
-                                     int64_t bucket_elems, void* stream) {
-  const char* fn = "zero_step_amp";
-  NvtxRange nvtx_range(fn);
-  clear_error();
+namespace zero {
+namespace {
+
+// The mixed-precision step: with `grads`, reduce-scatter them into the fp32
+// shards while summing squares (k_stats); without, the shards already hold
+// the reduced gradient (k_shard_stats).  Then the decision kernel and the
+// update (k_adamw_amp).
+zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* grads,
+                     zero_dtype dtype, zero_reduce_op op, float* const* grad_shards,
+                     float* const* master, float* const* m, float* const* v, void* full_flat16,
+                     void* const* out16_shard, const zero_adamw_hparams* hp,
+                     const zero_amp_config* cfg, void* d_state, void* workspace,
+                     int64_t workspace_bytes, uint64_t rank_mask, int64_t bucket_elems,
+                     void* stream) {
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
   if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
   ZERO_TRY(check_hparams(fn, hp, 1));
   ZERO_TRY(check_amp_config(fn, cfg));
-  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  if (grads) ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
   ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
@@ -559,7 +562,7 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
   if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
   LaunchArgs& a = *h.p;
   for (int r = 0; r < plan->n_ranks; ++r) {
-    a.grads[r] = grads[r];
+    a.grads[r] = grads ? grads[r] : nullptr;
     if (!in_mask(rank_mask, r)) continue;
     a.gshard[r] = grad_shards[r];
     a.master[r] = master[r];
@@ -578,15 +581,16 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
   a.beta1 = hp->beta1;
   a.beta2 = hp->beta2;
   set_scale(a, plan->n_ranks, op);
+  const Kind stats = grads ? Kind::kStats : Kind::kShardStats;
   int64_t done = 0;
-  ZERO_TRY(run_buckets(fn, Kind::kStats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
+  ZERO_TRY(run_buckets(fn, stats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
   if (done == 0) {
     // no owned element: one empty reduction launch still prepares the
     // decision kernel (beta powers, counter)
     a.n_jobs = 0;
     a.n_tiles = 0;
     a.tile_base = 0;
-    const int err = launch_kernel(Kind::kStats, dtype, a, stream);
+    const int err = launch_kernel(stats, dtype, a, stream);
     if (err != 0)
       return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                   cudaGetErrorString(static_cast<cudaError_t>(err)));
@@ -602,6 +606,42 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
                 cudaGetErrorString(static_cast<cudaError_t>(err)));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return run_buckets(fn, Kind::kAdamwAmp, dtype, plan, rank_mask, 0, a, stream);
+}
+
+}  // namespace
+}  // namespace zero
+
+extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* grads,
+                                     zero_dtype dtype, zero_reduce_op op,
+                                     float* const* grad_shards, float* const* master,
+                                     float* const* m, float* const* v, void* full_flat16,
+                                     void* const* out16_shard, const zero_adamw_hparams* hp,
+                                     const zero_amp_config* cfg, void* d_state, void* workspace,
+                                     int64_t workspace_bytes, uint64_t rank_mask,
+                                     int64_t bucket_elems, void* stream) {
+  const char* fn = "zero_step_amp";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  if (!grads) return fail(ZERO_ERR_INVALID, "%s: grads is NULL", fn);
+  return amp_step(fn, plan, grads, dtype, op, grad_shards, master, m, v, full_flat16, out16_shard,
+                  hp, cfg, d_state, workspace, workspace_bytes, rank_mask, bucket_elems, stream);
+}
+
+extern "C" zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dtype,
+                                            float* const* grad_shards, float* const* master,
+                                            float* const* m, float* const* v,
+                                            void* full_flat16, void* const* out16_shard,
+                                            const zero_adamw_hparams* hp,
+                                            const zero_amp_config* cfg, void* d_state,
+                                            void* workspace, int64_t workspace_bytes,
+                                            uint64_t rank_mask, int64_t bucket_elems,
+                                            void* stream) {
+  const char* fn = "zero_step_amp_shards";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  return amp_step(fn, plan, nullptr, dtype, ZERO_REDUCE_SUM, grad_shards, master, m, v,
+                  full_flat16, out16_shard, hp, cfg, d_state, workspace, workspace_bytes,
+                  rank_mask, bucket_elems, stream);
 }
 
 namespace {

@@ -132,7 +132,7 @@ struct LaunchArgs {
   Job jobs[kMaxJobs];
 };
 
-enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kAdamwAmp };
+enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kShardStats, kAdamwAmp };
 
 // The decision of a mixed-precision step as the update kernel needs it.  The
 // decision kernel writes kAmpCopies copies, 64 bytes apart, at the start of

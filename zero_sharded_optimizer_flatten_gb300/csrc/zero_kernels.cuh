@@ -632,14 +632,15 @@ __device__ __forceinline__ void tile_sum_barrier(SqSum s, SqSum* warp_part, Norm
   __syncthreads();
 }
 
-// Reduce-scatter into fp32 shards plus, per tile, the sum of the binary32
-// squares of the reduced gradient (SqSum; a non-finite gradient makes it
-// non-finite).  One tile per CTA (the usual launch): the per-tile sum needs
-// no barrier (tile_sum_last_warp); if the grid ever strides over several
-// tiles, the block-wide barrier version is used.
-template <class T, int NR>
-__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
-  grid_dependency_begin();
+// Per tile, the sum of the binary32 squares of the reduced gradient (SqSum; a
+// non-finite gradient makes it non-finite).  Reduce = true: the tile is first
+// reduce-scattered from the replicas into the fp32 shards (k_stats);
+// Reduce = false: the shards already hold the reduced gradient, which is only
+// read (k_shard_stats).  One tile per CTA (the usual launch): the per-tile
+// sum needs no barrier (tile_sum_last_warp); if the grid ever strides over
+// several tiles, the block-wide barrier version is used.
+template <class T, int NR, bool Reduce>
+__device__ __forceinline__ void stats_tiles(const LaunchArgs& a) {
   __shared__ SqSum warp_part[kThreads / 32];
   __shared__ int arrived;
   const bool one_tile = static_cast<int64_t>(gridDim.x) >= a.n_tiles;
@@ -657,8 +658,12 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
       if (e0 < jb.len && access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec))) {
         const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
         float g[8];
-        reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
-        store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
+        if constexpr (Reduce) {
+          reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
+          store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
+        } else {
+          load_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k) s.add(__fmul_rn(g[k], g[k]));
       }
@@ -667,8 +672,13 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
       for (int k = 0; k < kTile / kThreads; ++k) {
         const int64_t e = base + k * kThreads + threadIdx.x;
         if (e < jb.len && access_ok(a, jb, e, 1)) {
-          const float g = reduce1<T, NR>(a, jb.flat_off + e);
-          a.gshard[jb.rank][jb.shard_off + e] = g;
+          float g;
+          if constexpr (Reduce) {
+            g = reduce1<T, NR>(a, jb.flat_off + e);
+            a.gshard[jb.rank][jb.shard_off + e] = g;
+          } else {
+            g = a.gshard[jb.rank][jb.shard_off + e];
+          }
           s.add(__fmul_rn(g, g));
         }
       }
@@ -690,6 +700,18 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __gri
     a.head->beta_pow[1] = pow(a.beta2, t);
     a.head->arrived = 0;
   }
+}
+
+template <class T, int NR>
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
+  stats_tiles<T, NR, true>(a);
+}
+
+template <class T>
+__global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_shard_stats(const __grid_constant__ LaunchArgs a) {
+  grid_dependency_begin();
+  stats_tiles<T, 1, false>(a);
 }
 
 // AdamW + cast + all-gather on the reduced fp32 gradient times the decision
@@ -805,12 +827,14 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kAllgather: fn = reinterpret_cast<const void*>(&k_allgather<T>); break;
     case Kind::kInit: fn = reinterpret_cast<const void*>(&k_init<T>); break;
     case Kind::kStats: fn = by_ranks<T, PickStats>(a.n_ranks); break;
+    case Kind::kShardStats: fn = reinterpret_cast<const void*>(&k_shard_stats<T>); break;
     case Kind::kAdamwAmp: fn = reinterpret_cast<const void*>(&k_adamw_amp<T>); break;
   }
   const int64_t units = kind == Kind::kAllgather ? (a.n_tiles + kGatherTiles - 1) / kGatherTiles
                                                  : a.n_tiles;
   int grid = grid_for(fn, units);
-  if (kind == Kind::kStats && grid == 0) grid = 1;  // an empty launch still prepares the decision
+  if ((kind == Kind::kStats || kind == Kind::kShardStats) && grid == 0)
+    grid = 1;  // an empty launch still prepares the decision
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
   return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args, 0, s));

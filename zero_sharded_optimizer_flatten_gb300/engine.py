@@ -17,6 +17,14 @@ describe the optimizer doing it:
   casts to 16 bits and all-gathers into the flat buffer, so the model's
   parameters hold the new values.
 
+With ``amp`` (an ``AmpConfig``) the engine is the fp16 ZeRO-2 loop of the
+pages' ds_config (fp16 loss_scale 0 = dynamic, loss_scale_window,
+hysteresis, min_loss_scale, gradient_clipping): ``backward`` multiplies each
+rank's loss by the current loss scale, read on the device from the state
+buffer (no host synchronisation), and ``step()`` runs the mixed-precision
+step on the reduced shards (overflow skip, scale update, clipping, AdamW,
+cast, gather; ``zero_step_amp_shards``).
+
 The arithmetic is the library's (no compute happens here); this module only
 does bookkeeping and launches.
 """
@@ -32,7 +40,8 @@ from . import zero as Z
 class ZeroEngine:
     def __init__(self, params: Iterable[torch.nn.Parameter], n_ranks: int, *, mode="flat",
                  align: int = 16, op: str = "avg", hparams: Optional[Z.AdamW] = None,
-                 bucket_elems: int = 50_000_000, overlap_comm: bool = True):
+                 bucket_elems: int = 50_000_000, overlap_comm: bool = True,
+                 amp: Optional[Z.AmpConfig] = None):
         self.params: List[torch.nn.Parameter] = list(params)
         if not self.params:
             raise ValueError("no parameters")
@@ -81,6 +90,15 @@ class ZeroEngine:
             self._tensor_buckets.append(parts)
         self.reduction_stream = torch.cuda.Stream(dev) if overlap_comm else None
         self._reduce = Z.ReduceScatterRange(plan, self.grads, op, self.grad_shards)
+        # mixed-precision controls: device state, its loss scale as a tensor
+        # view (the state's first field), the step's workspace
+        self.amp = amp
+        if amp is not None:
+            self.amp_state = Z.amp_state_tensor(dev)
+            Z.zero_amp_init(self.amp_state, amp)
+            self._scale = self.amp_state[:8].view(torch.float64)[0]
+            self._workspace = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan)),
+                                          dtype=torch.uint8, device=dev)
         self.step_count = 0
         self.launched_during_backward = 0
         self._current: Optional[int] = None
@@ -132,6 +150,8 @@ class ZeroEngine:
             raise RuntimeError(f"rank {rank} already ran backward in this iteration")
         self._current = rank
         try:
+            if self.amp is not None:
+                loss = loss * self._scale.to(loss.dtype)
             loss.backward()
         finally:
             self._current = None
@@ -152,10 +172,24 @@ class ZeroEngine:
         if self.reduction_stream is not None:
             torch.cuda.current_stream().wait_stream(self.reduction_stream)
         self.step_count += 1
-        Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
-                                self.shard16, self.hp, self.step_count)
-        Z.zero_allgather(self.plan, self.shard16, self.flat16)
+        if self.amp is not None:
+            # the step count that AdamW uses lives in the device state (skipped
+            # steps do not count)
+            Z.zero_step_amp_shards(self.plan, self.grad_shards, self.master, self.m, self.v,
+                                   self.flat16, None, self.hp, self.amp, self.amp_state,
+                                   self._workspace)
+        else:
+            Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
+                                    self.shard16, self.hp, self.step_count)
+            Z.zero_allgather(self.plan, self.shard16, self.flat16)
         self._reset()
+
+    def amp_status(self) -> "Z.AmpState":
+        """The mixed-precision state (loss scale, last norm, steps taken and
+        skipped); copying it to the host synchronises with the stream."""
+        if self.amp is None:
+            raise RuntimeError("the engine was built without amp")
+        return Z.read_amp_state(self.amp_state)
 
     def remove_hooks(self):
         for h in self._hooks:

@@ -97,6 +97,8 @@ def lib():
                 "zero_amp_workspace_bytes": [vp, u64, i64, i64p],
                 "zero_step_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp, vp,
                                   vpp, hp, ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
+                "zero_step_amp_shards": [vp, ctypes.c_int, vpp, vpp, vpp, vpp, vp, vpp, hp,
+                                         ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
                 "zero_step_amp_noalloc": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp,
                                           vpp, vp, vpp, hp, ctypes.POINTER(AmpConfigC), vp, u64,
                                           i64, vp],
@@ -524,6 +526,41 @@ def zero_step_amp(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
                            _ptrs(vv), full, o16, ctypes.byref(hp), ctypes.byref(c),
                            _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
                            int(bucket_elems), _stream(stream)))
+
+
+def zero_step_amp_shards(plan: Plan, grad_shards, master, m, v, full_flat16, out16_shard,
+                         hparams: AdamW, cfg: AmpConfig, d_state, workspace, rank_mask=None,
+                         bucket_elems=0, stream=None, dtype=None):
+    """The mixed-precision step from already reduce-scattered fp32 gradient
+    shards (read only): loss-scale check, clipping, AdamW, cast, gather.
+    ``dtype`` (the 16-bit format) defaults to that of ``full_flat16`` or of
+    the first ``out16_shard`` tensor."""
+    torch = _torch()
+    L = lib()
+    mask = _mask(plan, rank_mask)
+    ext = plan.flat_extent(mask)
+    if dtype is None:
+        seq = [full_flat16] + (list(out16_shard) if out16_shard is not None else [])
+        dt = _sixteen([t for t in seq if t is not None] or [None])
+    else:
+        dt = dtype
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    o16 = (_ptrs(_per_rank(plan, out16_shard, "out16_shard", mask, nullable=True))
+           if out16_shard is not None else None)
+    need = zero_amp_workspace_bytes(plan, mask, bucket_elems)
+    ws_bytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) \
+        else need
+    ws = _addr(workspace, "workspace")
+    hp = hparams.c()
+    c = cfg.c()
+    _check(L.zero_step_amp_shards(plan.handle, dt, _ptrs(gs), _ptrs(ms), _ptrs(mm), _ptrs(vv),
+                                  full, o16, ctypes.byref(hp), ctypes.byref(c),
+                                  _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
+                                  int(bucket_elems), _stream(stream)))
 
 
 def zero_step_amp_noalloc(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
