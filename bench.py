@@ -353,7 +353,7 @@ class FlatRunner:
     (bucketed if the workload says so).  Gradient buffers hold only the flat
     range the masked ranks own."""
 
-    def __init__(self, w, dev, grad_sets, amp=None, offload=False):
+    def __init__(self, w, dev, grad_sets, amp=None, offload=False, from_shards=False):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
@@ -407,6 +407,20 @@ class FlatRunner:
             # reduction pass 2N + 4 B, update pass 4 + 24 + 2 B per element
             self.bytes_per_step = (2 * w.n_ranks + 34) * self.elems
             self.kernel = "k_stats + k_amp_finalize + k_adamw_amp"
+        if amp is not None and from_shards:
+            # the gradients arrive reduce-scattered (as a training loop's
+            # overlapped bucket reductions leave them): reduce once, untimed
+            Z.zero_reduce_scatter(plan, self.grads[0], w.op, self.gsh, rank_mask=self.mask,
+                                  bucket_elems=w.bucket_elems)
+
+            def step_shards(t):
+                Z.zero_step_amp_shards(plan, self.gsh, self.master, self.m, self.v, self.full16,
+                                       None, self.hp, amp, self.state, self.ws,
+                                       rank_mask=self.mask, bucket_elems=w.bucket_elems)
+            self.calls = [step_shards]
+            # shard read 4 B, update pass 4 + 24 + 2 B per element
+            self.bytes_per_step = 34 * self.elems
+            self.kernel = "k_shard_stats + k_amp_finalize + k_adamw_amp"
 
     def step(self, t, events=None):
         if events is not None:
@@ -556,7 +570,7 @@ def run_gpu(args, world, rank, local):
         if args.amp:
             amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
                               max_norm=args.max_norm)
-        run = FlatRunner(w, dev, args.grad_sets, amp, args.offload)
+        run = FlatRunner(w, dev, args.grad_sets, amp, args.offload, args.from_shards)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -945,6 +959,7 @@ def run_engine(args, world, rank, local):
     without overlapping the bucket reduce-scatters with the backward pass."""
     import torch
 
+    import zero_sharded_optimizer_flatten_gb300 as Z
     from zero_sharded_optimizer_flatten_gb300.engine import ZeroEngine
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -960,10 +975,12 @@ def run_engine(args, world, rank, local):
     N = 4
     xs = [torch.randn(args.tokens, 1024, device=dev, dtype=torch.bfloat16) for _ in range(N)]
     out = {}
+    amp = (Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
+                       max_norm=args.max_norm) if args.amp else None)
     for overlap in (False, True):
         model = toy()
         eng = ZeroEngine(model.parameters(), N, mode="round_robin", op="sum",
-                         bucket_elems=args.bucket, overlap_comm=overlap)
+                         bucket_elems=args.bucket, overlap_comm=overlap, amp=amp)
 
         def iteration():
             for q in range(N):
@@ -988,7 +1005,8 @@ def run_engine(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": out["overlap"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "ToyModel hidden 1024 x12 + Linear(1024,10), round-robin N=4",
+            "config": {"workload": "ToyModel hidden 1024 x12 + Linear(1024,10), round-robin N=4"
+                                   + (", mixed precision (loss scale, clipping)" if amp else ""),
                        "phi": phi, "tokens_per_rank": args.tokens, "bucket_elems": args.bucket,
                        "ms_per_iteration": {"serial": out["serial"], "overlap": out["overlap"]},
                        "bucket_launches_during_backward": out["launched_during_backward"]}}
@@ -1016,6 +1034,9 @@ def main(argv=None):
     ap.add_argument("--amp", action="store_true",
                     help="time the mixed-precision step (norm check + clipping) instead")
     ap.add_argument("--max-norm", type=float, default=1.0)
+    ap.add_argument("--from-shards", action="store_true",
+                    help="--amp: the step from already reduce-scattered fp32 gradient shards "
+                         "(zero_step_amp_shards)")
     ap.add_argument("--offload", action="store_true",
                     help="keep the fp32 optimizer state in pinned host memory (ZeRO-Offload "
                          "over the host link)")

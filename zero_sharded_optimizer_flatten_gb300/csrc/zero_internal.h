@@ -62,6 +62,16 @@ constexpr int kGatherTiles = ZERO_GATHER_TILES;
 #define ZERO_PDL 0
 #endif
 
+// Consecutive 2048-element tiles one CTA of the shard-only sum of squares
+// (k_shard_stats) reads.  Measured on the BERT-base group (mixed-precision
+// step from reduced shards): 1 / 2 / 4 / 8 tiles 613 / 598 / 602 / 657 us
+// per step; a persistent grid that prefetches the next two tiles while
+// reducing the current ones took 160 us per launch against 127 us for 2.
+#ifndef ZERO_SHARD_STATS_TILES
+#define ZERO_SHARD_STATS_TILES 2
+#endif
+constexpr int kShardStatsTiles = ZERO_SHARD_STATS_TILES;
+
 // Bounds-checked build: every kernel access is checked against the plan's
 // buffer lengths; a violation skips the access and sets the device error
 // word to 2 (zero_sync reports it).

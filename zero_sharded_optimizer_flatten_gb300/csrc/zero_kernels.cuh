@@ -632,14 +632,26 @@ __device__ __forceinline__ void tile_sum_barrier(SqSum s, SqSum* warp_part, Norm
   __syncthreads();
 }
 
-// Per tile, the sum of the binary32 squares of the reduced gradient (SqSum; a
-// non-finite gradient makes it non-finite).  Reduce = true: the tile is first
-// reduce-scattered from the replicas into the fp32 shards (k_stats);
-// Reduce = false: the shards already hold the reduced gradient, which is only
-// read (k_shard_stats).  One tile per CTA (the usual launch): the per-tile
-// sum needs no barrier (tile_sum_last_warp); if the grid ever strides over
-// several tiles, the block-wide barrier version is used.
-template <class T, int NR, bool Reduce>
+// The launch holding the step's first tile also prepares the decision
+// kernel: beta1^t and beta2^t of the step t = step + 1 that an update would
+// take (binary64 pow, here off the decision's critical path), and a zero
+// arrival counter.  The decision kernel runs after every launch of the
+// reduction has completed.
+__device__ __forceinline__ void prepare_decision(const LaunchArgs& a) {
+  if (a.head && a.tile_base == 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+    const double t = static_cast<double>(a.amp_state->step + 1);
+    a.head->beta_pow[0] = pow(a.beta1, t);
+    a.head->beta_pow[1] = pow(a.beta2, t);
+    a.head->arrived = 0;
+  }
+}
+
+// Reduce-scatter into fp32 shards plus, per tile, the sum of the binary32
+// squares of the reduced gradient (SqSum; a non-finite gradient makes it
+// non-finite).  One tile per CTA (the usual launch): the per-tile sum needs
+// no barrier (tile_sum_last_warp); if the grid ever strides over several
+// tiles, the block-wide barrier version is used.
+template <class T, int NR>
 __device__ __forceinline__ void stats_tiles(const LaunchArgs& a) {
   __shared__ SqSum warp_part[kThreads / 32];
   __shared__ int arrived;
@@ -658,12 +670,8 @@ __device__ __forceinline__ void stats_tiles(const LaunchArgs& a) {
       if (e0 < jb.len && access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec))) {
         const int64_t f0 = jb.flat_off + e0, i0 = jb.shard_off + e0;
         float g[8];
-        if constexpr (Reduce) {
-          reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
-          store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
-        } else {
-          load_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
-        }
+        reduce_quads<T, NR>(a, f0, f0 + kHalf, two, g);
+        store_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g);
 #pragma unroll
         for (int k = 0; k < 8; ++k) s.add(__fmul_rn(g[k], g[k]));
       }
@@ -672,13 +680,8 @@ __device__ __forceinline__ void stats_tiles(const LaunchArgs& a) {
       for (int k = 0; k < kTile / kThreads; ++k) {
         const int64_t e = base + k * kThreads + threadIdx.x;
         if (e < jb.len && access_ok(a, jb, e, 1)) {
-          float g;
-          if constexpr (Reduce) {
-            g = reduce1<T, NR>(a, jb.flat_off + e);
-            a.gshard[jb.rank][jb.shard_off + e] = g;
-          } else {
-            g = a.gshard[jb.rank][jb.shard_off + e];
-          }
+          const float g = reduce1<T, NR>(a, jb.flat_off + e);
+          a.gshard[jb.rank][jb.shard_off + e] = g;
           s.add(__fmul_rn(g, g));
         }
       }
@@ -689,29 +692,81 @@ __device__ __forceinline__ void stats_tiles(const LaunchArgs& a) {
     else
       tile_sum_barrier(s, warp_part, out);
   }
-  // The launch holding the step's first tile also prepares the decision
-  // kernel: beta1^t and beta2^t of the step t = step + 1 that an update would
-  // take (binary64 pow, here off the decision's critical path), and a zero
-  // arrival counter.  The decision kernel runs after every launch of this
-  // kernel has completed.
-  if (a.head && a.tile_base == 0 && blockIdx.x == 0 && threadIdx.x == 0) {
-    const double t = static_cast<double>(a.amp_state->step + 1);
-    a.head->beta_pow[0] = pow(a.beta1, t);
-    a.head->beta_pow[1] = pow(a.beta2, t);
-    a.head->arrived = 0;
-  }
+  prepare_decision(a);
 }
 
 template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
   grid_dependency_begin();
-  stats_tiles<T, NR, true>(a);
+  stats_tiles<T, NR>(a);
 }
 
+// Per-tile sums of squares of gradients already reduced into the fp32
+// shards (one 4-byte read per element).  Reading 8 KB per tile is too little
+// to amortise a CTA, so a CTA takes kShardStatsTiles consecutive tiles: every
+// load first, then each tile's sum in the same order as stats_tiles (a
+// thread's elements in order, the warp's shuffle tree, the warps in index
+// order), so the partials are bit-identical to those of k_stats on the same
+// tiles.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_shard_stats(const __grid_constant__ LaunchArgs a) {
   grid_dependency_begin();
-  stats_tiles<T, 1, false>(a);
+  constexpr int K = kShardStatsTiles;
+  __shared__ SqSum warp_part[K][kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * K; t0 < a.n_tiles;
+       t0 += static_cast<int64_t>(gridDim.x) * K) {
+    int job[K];
+    bool quads[K];
+    float g[K][8];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t tile = t0 + k;
+      job[k] = tile < a.n_tiles ? find_job(a, tile) : -1;
+      quads[k] = false;
+      if (job[k] < 0) continue;
+      const Job& jb = a.jobs[job[k]];
+      if (!jb.vec) continue;
+      const int64_t e0 = (tile - jb.tile_begin) * kTile + static_cast<int64_t>(threadIdx.x) * kVec;
+      const bool two = e0 + kHalf < jb.len;
+      if (e0 < jb.len && access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec))) {
+        const int64_t i0 = jb.shard_off + e0;
+        load_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g[k]);
+        quads[k] = true;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      SqSum s = sq_zero();
+      if (job[k] >= 0) {
+        const Job& jb = a.jobs[job[k]];
+        if (quads[k]) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s.add(__fmul_rn(g[k][e], g[k][e]));
+        } else if (!jb.vec) {
+          const int64_t base = (t0 + k - jb.tile_begin) * kTile;
+#pragma unroll 1
+          for (int e = 0; e < kTile / kThreads; ++e) {
+            const int64_t x = base + e * kThreads + threadIdx.x;
+            if (x < jb.len && access_ok(a, jb, x, 1)) {
+              const float v = a.gshard[jb.rank][jb.shard_off + x];
+              s.add(__fmul_rn(v, v));
+            }
+          }
+        }
+      }
+      s = warp_sum(s);
+      if (lane == 0) warp_part[k][warp] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < K && t0 + threadIdx.x < a.n_tiles) {
+      SqSum t = warp_part[threadIdx.x][0];
+      for (int w = 1; w < kThreads / 32; ++w) t.add(warp_part[threadIdx.x][w]);
+      store_partial(a.partials + a.tile_base + t0 + threadIdx.x, t);
+    }
+    __syncthreads();
+  }
+  prepare_decision(a);
 }
 
 // AdamW + cast + all-gather on the reduced fp32 gradient times the decision
@@ -830,8 +885,10 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     case Kind::kShardStats: fn = reinterpret_cast<const void*>(&k_shard_stats<T>); break;
     case Kind::kAdamwAmp: fn = reinterpret_cast<const void*>(&k_adamw_amp<T>); break;
   }
-  const int64_t units = kind == Kind::kAllgather ? (a.n_tiles + kGatherTiles - 1) / kGatherTiles
-                                                 : a.n_tiles;
+  const int64_t units =
+      kind == Kind::kAllgather    ? (a.n_tiles + kGatherTiles - 1) / kGatherTiles
+      : kind == Kind::kShardStats ? (a.n_tiles + kShardStatsTiles - 1) / kShardStatsTiles
+                                  : a.n_tiles;
   int grid = grid_for(fn, units);
   if ((kind == Kind::kStats || kind == Kind::kShardStats) && grid == 0)
     grid = 1;  // an empty launch still prepares the decision

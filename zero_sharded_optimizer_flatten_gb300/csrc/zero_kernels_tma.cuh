@@ -223,7 +223,7 @@ struct PickStepTma {
 
 // Persistent grid: resident CTAs per SM (given the stage ring's shared
 // memory) times the SM count, capped by the tile count.
-int tma_grid(const void* fn, int smem_bytes, int64_t n_tiles);
+int resident_grid(const void* fn, int smem_bytes, int64_t n_tiles);
 
 template <class T>
 int launch_step_tma_impl(const LaunchArgs& a, cudaStream_t s) {
@@ -240,7 +240,7 @@ int launch_step_tma_impl(const LaunchArgs& a, cudaStream_t s) {
     default: fn = PickStepTma<T, 8>::get(); smem = tma_stage_bytes<8>(); break;
   }
   smem *= kTmaStages;
-  const int grid = tma_grid(fn, smem, a.n_tiles);
+  const int grid = resident_grid(fn, smem, a.n_tiles);
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
   return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args,

@@ -160,7 +160,9 @@ int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* str
   return static_cast<int>(cudaGetLastError());
 }
 
-int tma_grid(const void* fn, int smem_bytes, int64_t n_tiles) {
+// A persistent grid for `fn`: as many CTAs as fit on the GPU at once (with
+// smem_bytes of dynamic shared memory each), but no more than n_tiles.
+int resident_grid(const void* fn, int smem_bytes, int64_t n_tiles) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   static std::mutex mu;
