@@ -162,3 +162,45 @@ def test_engine_mixed_precision_step_and_training():
     assert st.scale < 2.0 ** 24
     assert curve[-1] < 0.5 * curve[0], (curve[0], curve[-1])
     eng.remove_hooks()
+
+
+@pytest.mark.parametrize("mode,overlap,bucket", [("round_robin", True, 20_000),
+                                                 ("flat", False, 20_000),
+                                                 ("flat", True, 0)])
+def test_engine_mixed_precision_step_other_layouts(mode, overlap, bucket):
+    """The engine's fp16 step equals zero_step_amp on copies of its replicas
+    and state, bit for bit, for round-robin ownership, without overlap and
+    with one bucket; 8 iterations from a scale of 2^20 (skips included)."""
+    teacher = _mlp(321, torch.float32)
+    student = _mlp(2, torch.float16)
+    cfg = Z.AmpConfig(init_scale=2.0 ** 20, min_scale=1.0, window=3, hysteresis=2,
+                      max_norm=0.5)
+    hp = Z.AdamW(2e-3, 0.9, 0.99, 1e-8, 0.05)
+    eng = ZeroEngine(student.parameters(), N, mode=mode, align=16, op="avg", hparams=hp,
+                     bucket_elems=bucket, overlap_comm=overlap, amp=cfg)
+    for t in range(8):
+        xs = [_micro_batch(q, 100 + t) for q in range(N)]
+        for q in range(N):
+            with torch.no_grad():
+                y = teacher(xs[q])
+            eng.backward((student(xs[q].to(torch.float16)).float() - y).pow(2).mean(), q)
+        if eng.reduction_stream is not None:
+            torch.cuda.current_stream().wait_stream(eng.reduction_stream)
+        grads = [g.clone() for g in eng.grads]
+        copies = {k: [x.clone() for x in getattr(eng, k)] for k in ("master", "m", "v")}
+        state = eng.amp_state.clone()
+        flat = eng.flat16.clone()
+        gsh = [torch.empty_like(x) for x in eng.grad_shards]
+        ws = torch.empty_like(eng._workspace)
+        Z.zero_step_amp(eng.plan, grads, "avg", gsh, copies["master"], copies["m"],
+                        copies["v"], flat, None, hp, cfg, state, ws)
+        eng.step()
+        torch.cuda.synchronize()
+        assert torch.equal(state, eng.amp_state), t
+        assert torch.equal(flat.view(torch.int16), eng.flat16.view(torch.int16)), t
+        for k in ("master", "m", "v"):
+            for r in range(N):
+                assert torch.equal(copies[k][r].view(torch.int32),
+                                   getattr(eng, k)[r].view(torch.int32)), (t, k, r)
+    assert eng.amp_status().step >= 1
+    eng.remove_hooks()
