@@ -494,8 +494,19 @@ int orc_allgather(const int64_t* numel, int32_t n_tensors, int32_t N, int32_t mo
  * 1000, hysteresis 2, min_loss_scale 1; gradient_clipping).  Reading taken:
  *  - the gradients carry the loss scale S; the reduced gradient g (sum or
  *    average of the replicas, as in the plain step) is checked for
- *    non-finite values through its squared norm  sumsq = sum g^2  (each
- *    square rounded to binary32, the sum taken in binary64);
+ *    non-finite values through its squared norm  sumsq = sum g^2.  Each
+ *    square is the binary32 product g*g: the setup the pages configure is
+ *    fp16 training with binary32 gradients and master weights (ds_config
+ *    fp16 block with amp opt_level O2, "ZeRO ... 实操" §3.3; the fp32
+ *    optimizer partition, "DeepSpeed ZeRO-2 ..." §2.1), where the gradient
+ *    and every operation on it are binary32 -- the same rule the update
+ *    below follows, whose second moment forms this very product.  The
+ *    squares are added in binary64, so that (up to binary64 rounding, far
+ *    below the rounding of one binary32 square) the sum does not depend on
+ *    how the elements are partitioned over ranks or ordered: partitioning
+ *    must leave the result unchanged ("ZeRO ... 实操" §2.1, partitioning
+ *    changes no dtype or shape).  So sumsq is non-finite exactly when some
+ *    g is non-finite or |g| >= 2^64 (its binary32 square overflows);
  *  - non-finite sumsq: the update is skipped (no state, parameter or step
  *    count changes); if more than one overflow is still tolerated the
  *    tolerance drops by one, else S halves (not below min_scale); the

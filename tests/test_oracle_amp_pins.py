@@ -2,6 +2,8 @@
 global-norm clipping) to facts outside itself: the plain step it must reduce
 to, exact power-of-two scaling, torch's clip_grad_norm_ + AdamW, and the
 loss-scale trajectory the configuration keys describe."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -12,10 +14,15 @@ from zero_sharded_optimizer_flatten_gb300 import workloads as W
 NUMEL = (1000, 37, 4096, 3, 129)
 
 
+def _flat_len(w):
+    mode = oracle.FLAT if w.mode == "flat" else oracle.ROUND_ROBIN
+    return oracle.flat_len(list(w.numel), w.n_ranks, mode, w.align)
+
+
 def _setup(w):
     mode = oracle.FLAT if w.mode == "flat" else oracle.ROUND_ROBIN
     dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
-    p16 = W.params16(w, "cpu").view(torch.int16).numpy().view(np.uint16)
+    p16 = W.params16(w, "cpu", _flat_len(w)).view(torch.int16).numpy().view(np.uint16)
     master, m, v = [], [], []
     for r in range(w.n_ranks):
         seg = oracle.segments(list(w.numel), w.n_ranks, mode, w.align, r)
@@ -26,14 +33,14 @@ def _setup(w):
         master.append(mst)
         m.append(np.zeros(S, np.float32))
         v.append(np.zeros(S, np.float32))
-    return mode, dt, master, m, v, np.zeros(W.flat_len(w), np.uint16)
+    return mode, dt, master, m, v, np.zeros(_flat_len(w), np.uint16)
 
 
 def _grads(w, t, scale=1.0):
     """Replicas drawn in binary32, multiplied by `scale`, rounded to 16 bits."""
     out = []
     for q in range(w.n_ranks):
-        x = W.grads16(w, t, q, "cpu").float() * scale
+        x = W.grads16(w, t, q, "cpu", 0, _flat_len(w)).float() * scale
         out.append(x.to(w.torch_dtype).view(torch.int16).numpy().view(np.uint16))
     return out
 
@@ -166,3 +173,85 @@ def test_scale_grows_every_window_of_good_steps():
     # closed form: S after k good steps = S0 * 2^floor(k / window)
     assert scales == [8.0 * 2 ** (k // 3) for k in range(1, 8)]
     assert st.step == 7 and st.good_steps == 1 and st.hysteresis_left == 2
+
+
+# ----------------------------------------------------------------------------
+# the squared norm: binary32 squares of the reduced gradient, summed in binary64
+#
+# Reading (the pages give only the fp16 / gradient_clipping configuration
+# keys, "ZeRO ... 实操" (wmrh.cn) §3.1, §3.3): the reduced gradient and
+# every operation on it are binary32 (fp16 training with fp32 gradients and
+# master weights), so each square g*g is the binary32 product -- the same
+# product the second-moment update forms; the squares are added in binary64
+# so that the norm does not depend on the partition or the order.  Each pin
+# below fails under the other plausible readings: exact (binary64) squares,
+# or a binary32 sum.
+
+
+def _norm_case(values_by_rank, dtype, op=oracle.SUM, max_norm=0.0):
+    """One step of the oracle's mixed-precision step on a single tensor whose
+    replicas hold the given 16-bit values (binary64 numbers, exact in the
+    format); returns the state after it."""
+    N = len(values_by_rank)
+    n = len(values_by_rank[0])
+    td = torch.float16 if dtype == oracle.FP16 else torch.bfloat16
+    g = []
+    for vals in values_by_rank:
+        t = torch.tensor(vals, dtype=torch.float64)
+        h = t.to(td)
+        assert torch.equal(h.double(), t), "value not exact in the 16-bit format"
+        g.append(h.view(torch.int16).numpy().view(np.uint16).copy())
+    L = oracle.flat_len([n], N, oracle.FLAT, 16)
+    g = [np.concatenate([x, np.zeros(L - n, np.uint16)]) for x in g]
+    master, m, v = [], [], []
+    for r in range(N):
+        S = oracle.shard_len([n], N, oracle.FLAT, 16, r)
+        master.append(np.zeros(S, np.float32))
+        m.append(np.zeros(S, np.float32))
+        v.append(np.zeros(S, np.float32))
+    cfg = oracle.amp_config(init_scale=1.0, window=0, hysteresis=1, max_norm=max_norm)
+    st = oracle.amp_init(cfg)
+    oracle.step_amp([n], N, oracle.FLAT, 16, dtype, op, g, master, m, v,
+                    np.zeros(L, np.uint16), None, oracle.hparams(), cfg, st)
+    return st
+
+
+def test_norm_squares_are_binary32_products():
+    """Replicas 1 and 2^-12 sum to g = 1 + 2^-12 (exact in binary32); its
+    exact square 1 + 2^-11 + 2^-24 is a tie in binary32 and rounds to the
+    even 1 + 2^-11.  Over 4096 elements the squared norm is 4096 + 2 exactly;
+    exact squares would give 4096 + 2 + 2^-12."""
+    n = 4096
+    st = _norm_case([[1.0] * n, [2.0 ** -12] * n], oracle.FP16)
+    assert st.overflow == 0 and st.step == 1
+    assert st.norm == math.sqrt(n + 2)
+    assert st.norm != math.sqrt(n + 2 + 2.0 ** -12)
+    assert abs(math.sqrt(n + 2 + 2.0 ** -12) - math.sqrt(n + 2)) > 1e-9 * st.norm
+
+
+def test_norm_sum_is_binary64():
+    """One element 2^12 (square 2^24) then 1000 elements 1: a binary32 running
+    sum stays at 2^24 (each +1 is a tie that rounds back to even), the
+    binary64 sum is 2^24 + 1000 exactly."""
+    st = _norm_case([[4096.0] + [1.0] * 1000], oracle.FP16)
+    assert st.overflow == 0
+    assert st.norm == math.sqrt(2.0 ** 24 + 1000)
+
+
+def test_overflow_is_a_binary32_square_out_of_range():
+    """bf16 gradients: 2^63 squares to 2^126 (finite); 2^64 squares to 2^128,
+    beyond binary32, so the step is skipped as an overflow (its exact square
+    would be a finite binary64 number)."""
+    st = _norm_case([[2.0 ** 63] + [0.0] * 15], oracle.BF16)
+    assert st.overflow == 0 and st.norm == 2.0 ** 63
+    st = _norm_case([[2.0 ** 64] + [0.0] * 15], oracle.BF16)
+    assert st.overflow == 1 and st.step == 0 and st.skipped == 1
+
+
+def test_large_finite_squares_sum_beyond_binary32():
+    """Four bf16 gradients 1.5 x 2^63: each binary32 square 2.25 x 2^126 is
+    finite, their sum 9 x 2^126 is beyond binary32 but not binary64, so the
+    step is not an overflow and the norm is 3 x 2^63 exactly."""
+    st = _norm_case([[1.5 * 2.0 ** 63] * 4 + [0.0] * 12], oracle.BF16)
+    assert st.overflow == 0 and st.step == 1
+    assert st.norm == 3 * 2.0 ** 63
