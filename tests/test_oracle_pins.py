@@ -175,22 +175,32 @@ def test_round_robin_toy_model_shards():
 # memory model
 
 
-def _alloc_bytes_per_rank(stage, phi, N):
-    """Bytes a rank really allocates in the harness layout: 16-bit params and
-    grads (whole or this rank's shard), fp32 master/m/v shard."""
-    S = phi // N
-    params = np.empty(phi if stage < 3 else S, np.float16)
-    grads = np.empty(phi if stage < 2 else S, np.float16)
-    states = [np.empty(phi if stage == 0 else S, np.float32) for _ in range(3)]
-    return params.nbytes + grads.nbytes + sum(s.nbytes for s in states)
+def test_memory_model_closed_forms():
+    """The per-rank totals exactly as the pages print them (16Φ, 4Φ + 12Φ/N,
+    2Φ + 14Φ/N, 16Φ/N), as exact rationals over a grid of Φ and N that
+    includes N not dividing Φ; the table's rows must add up to its totals."""
+    g = json.load(open(os.path.join(GOLDEN, "memory_closed_forms.json")))
+    phis = [0, 1, 7, 1000, 4096 * 3 + 5, 109482240, 6738415616, 10 ** 12 + 39]
+    ranks = [1, 2, 3, 4, 5, 7, 8, 13, 64]
+    assert [c["stage"] for c in g["stages"]] == [0, 1, 2, 3]
+    for c in g["stages"]:
+        for k in ("whole", "split"):
+            assert c["params"][k] + c["grads"][k] + c["optimizer"][k] == c["total"][k]
+        assert c["total"]["whole"] + c["total"]["split"] == 16     # one rank holds 16 B/param
+        for phi in phis:
+            for N in ranks:
+                want = c["total"]["whole"] * phi + Fraction(c["total"]["split"] * phi, N)
+                assert Fraction(*oracle.memory_bytes(c["stage"], phi, N)) == want, \
+                    (c["name"], phi, N)
 
 
-def test_memory_model_against_allocations():
-    for stage in range(4):
-        for N in (1, 2, 4, 8):
-            phi = 4096 * 3
-            num, den = oracle.memory_bytes(stage, phi, N)
-            assert Fraction(num, den) == _alloc_bytes_per_rank(stage, phi, N)
+def test_memory_model_closed_forms_by_hand():
+    """The same forms at a few hand-worked points (Φ = 1000, N = 8):
+    16000, 4000 + 1500, 2000 + 1750, 2000 bytes; and Φ = 10, N = 3, where
+    N does not divide Φ: 160, 40 + 40, 20 + 140/3, 160/3."""
+    mb = lambda s, phi, N: Fraction(*oracle.memory_bytes(s, phi, N))  # noqa: E731
+    assert [mb(s, 1000, 8) for s in range(4)] == [16000, 5500, 3750, 2000]
+    assert [mb(s, 10, 3) for s in range(4)] == [160, 80, Fraction(200, 3), Fraction(160, 3)]
 
 
 def test_memory_model_worked_numbers():
@@ -362,11 +372,11 @@ def test_cast_of_update_is_rounding_of_master():
 
 def _run_sharded(w, steps, hp):
     """Oracle step over the plan with N virtual ranks."""
-    L = W.flat_len(w)
     mode = oracle.FLAT if w.mode == "flat" else oracle.ROUND_ROBIN
+    L = oracle.flat_len(list(w.numel), w.n_ranks, mode, w.align)
     dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
     op = oracle.AVG if w.op == "avg" else oracle.SUM
-    p16 = W.params16(w, "cpu").view(torch.int16).numpy().view(np.uint16)
+    p16 = W.params16(w, "cpu", L).view(torch.int16).numpy().view(np.uint16)
     shards = []
     for r in range(w.n_ranks):
         seg = oracle.segments(list(w.numel), w.n_ranks, mode, w.align, r)
@@ -377,7 +387,7 @@ def _run_sharded(w, steps, hp):
         shards.append((mst, np.zeros(S, np.float32), np.zeros(S, np.float32), seg))
     full = np.zeros(L, np.uint16)
     for t in range(1, steps + 1):
-        grads = [W.grads16(w, t, q, "cpu").view(torch.int16).numpy().view(np.uint16)
+        grads = [W.grads16(w, t, q, "cpu", 0, L).view(torch.int16).numpy().view(np.uint16)
                  for q in range(w.n_ranks)]
         oracle.step(list(w.numel), w.n_ranks, mode, w.align, dt, op, grads,
                     [s[0] for s in shards], [s[1] for s in shards], [s[2] for s in shards],
@@ -389,13 +399,15 @@ def _run_unsharded(w, steps, hp):
     """The same group as ONE flat buffer: reduce all N replicas, plain AdamW."""
     dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
     op = oracle.AVG if w.op == "avg" else oracle.SUM
-    p16 = W.params16(w, "cpu").view(torch.int16).numpy().view(np.uint16)
+    mode = oracle.FLAT if w.mode == "flat" else oracle.ROUND_ROBIN
+    L = oracle.flat_len(list(w.numel), w.n_ranks, mode, w.align)
+    p16 = W.params16(w, "cpu", L).view(torch.int16).numpy().view(np.uint16)
     master = oracle.to_f32(p16, dt)
     m, v = np.zeros_like(master), np.zeros_like(master)
     out = np.zeros(p16.size, np.uint16)
     for t in range(1, steps + 1):
-        grads = np.stack([W.grads16(w, t, q, "cpu").view(torch.int16).numpy().view(np.uint16)
-                          for q in range(w.n_ranks)])
+        grads = np.stack([W.grads16(w, t, q, "cpu", 0, L).view(torch.int16).numpy()
+                          .view(np.uint16) for q in range(w.n_ranks)])
         g = oracle.reduce_elements(grads, dt, op)
         oracle.adamw_elements(g, master, m, v, dt, hp, t, out16=out)
     return master, m, v, out
@@ -435,7 +447,7 @@ def test_unfused_composition_equals_step():
     p16, shards, full = _run_sharded(w, 1, hp)
     # recompute step 1 through the unfused pieces
     dt, mode = oracle.FP16, oracle.ROUND_ROBIN
-    grads = [W.grads16(w, 1, q, "cpu").view(torch.int16).numpy().view(np.uint16)
+    grads = [W.grads16(w, 1, q, "cpu", 0, full.size).view(torch.int16).numpy().view(np.uint16)
              for q in range(4)]
     outs, sh16 = [], []
     for r in range(4):
