@@ -1,9 +1,14 @@
 #!/usr/bin/env python
 """Benchmark of the fused ZeRO shard step on one GB300 (or N replicas).
 
-One step = one fused zero_step over all virtual ranks of the BERT-base-sized
-flat group: reduce-scatter of 8 bf16 gradient replicas, AdamW on the fp32
-master/m/v shards, bf16 cast and all-gather into the flat parameter buffer.
+One step = one fused zero_step over rank 0's 842M-element shard of the
+LLaMA-7B flat group (8 virtual ranks, 50M-element buckets, one launch per
+bucket): reduce-scatter of the 8 bf16 gradient slices, AdamW on the fp32
+master/m/v shard, bf16 cast and the write of the rank's slot of the flat
+parameter buffer.  It is the largest group of the path that fits one GPU.
+The same line carries `per_config`: the other groups (the tiny MLP back to
+back and with L2 flushed, BERT-base, the round-robin ToyModel, the 40-layer
+LLaMA-13B ZeRO-3 stream) measured in the same run.
 
 Prints one JSON line (rank 0).  `value` is whole-job params/s with inputs
 resident in HBM; `e2e` is the same metric through the public API with the
@@ -33,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "bert_base"
+WORKLOAD = "llama7b_rank0"
 METRIC = "fused ZeRO shard step: params/s and HBM GB/s (fraction of GB300 peak)"
 UNIT = "params/s"
 KERNEL_PREFIX = "k_step"
@@ -100,7 +105,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError) as e:
             self.error = f"nvidia-smi unavailable: {e}"
@@ -287,14 +292,22 @@ def host_cpu() -> dict:
 
 
 def cpu_baseline(w, budget_s: float = 10.0):
-    rate, _ = oracle_rate(w, 1 << 16)
-    n = int(min(w.phi, max(1 << 16, rate * budget_s)))
+    """The oracle on a bounded sample of the workload: one whole bucket for a
+    bucketed group (the unit one launch of the step processes), else about
+    `budget_s` seconds of single-threaded work."""
+    if w.bucket_elems:
+        n = int(min(w.phi, w.bucket_elems))
+        what = f"one whole {n}-element bucket (the first) of the {w.key} group"
+    else:
+        rate, _ = oracle_rate(w, 1 << 16)
+        n = int(min(w.phi, max(1 << 16, rate * budget_s)))
+        what = f"{n} elements of the {w.key} group"
     n -= n % 8
     sample = OracleSample(w, n)
     el = sample.step(1)
     out = {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
-           "sample": f"{n} elements of the {w.key} group (all {w.n_ranks} gradient replicas), "
-                     f"one step of the single-threaded C oracle, {el:.1f} s"}
+           "sample": f"{what} (all {w.n_ranks} gradient replicas), one step of the "
+                     f"single-threaded C oracle, {el:.1f} s"}
     # the same plain oracle over all host cores (element ranges split evenly)
     k = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
             else os.cpu_count() or 1)
@@ -500,11 +513,11 @@ class Zero3Runner:
         L = plan.padded
         S = [plan.shard_len(r) for r in range(w.n_ranks)]
         self.layer_buf = torch.empty(L, dtype=w.torch_dtype, device=dev)
-        self.grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+        self.grads = [W.grads16(w, 1, q, dev, 0, L) for q in range(w.n_ranks)]
         self.n_states = min(w.layers, layer_states)
         self.shards, self.calls, self.states = [], [], []
         for layer in range(self.n_states):
-            p16 = W.params16(w, dev, layer=layer)
+            p16 = W.params16(w, dev, L, layer=layer)
             sh = [p16[sum(S[:r]):sum(S[:r]) + S[r]].clone() for r in range(w.n_ranks)]
             master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
             m = [torch.empty_like(x) for x in master]
@@ -551,7 +564,174 @@ class Zero3Runner:
                 events[layer][1].record()
 
 
+# The other groups, measured in the same run as the headline and reported in
+# its `per_config` object: (key, workload, regime, options).  The tiny group
+# fits in L2, so it is reported twice: back to back from a CUDA graph (its
+# 36 MB stay in L2 between steps) and with L2 flushed before every step.
+PER_CONFIG = (
+    ("tiny_mlp/back_to_back", "tiny_mlp",
+     "back to back: the K steps captured in one CUDA graph and replayed once; the step's "
+     "36 MB stay in L2 between steps", dict(steps=2000, warmup=20)),
+    ("tiny_mlp/l2_flushed", "tiny_mlp",
+     "L2 flushed: a 256 MB buffer is read before every step, outside the step's events; "
+     "each step timed by its own events", dict(steps=300, warmup=5, flush_l2=True)),
+    ("bert_base", "bert_base",
+     "the K steps captured in one CUDA graph and replayed once; inputs larger than L2",
+     dict(steps=500, warmup=10)),
+    ("toy_rr", "toy_rr",
+     "the K steps captured in one CUDA graph and replayed once; inputs larger than L2",
+     dict(steps=500, warmup=10)),
+    ("llama13b_layer", "llama13b_layer",
+     "one step = one pass over the 40 layers through zero_zero3_pass (3 layer buffers, "
+     "gathers on a second stream); 40 distinct layer states; inputs larger than L2",
+     dict(steps=3, warmup=3, prefetch=3)),
+)
+
+
+def make_runner(w, dev, grad_sets=2, amp=None, offload=False, from_shards=False,
+                layer_states=40, prefetch=0):
+    if w.zero3:
+        return Zero3Runner(w, dev, layer_states, prefetch)
+    return FlatRunner(w, dev, grad_sets, amp, offload, from_shards)
+
+
+def time_steps(run, dev, steps, warmup, graph=True, flush_l2=False, dist=None, local=0, t=0):
+    """Warm up, then time `steps` steps of `run` on the current stream.
+
+    Flat groups: the timed steps are captured in one CUDA graph (each with its
+    own step number) and replayed once, unless `flush_l2`, which reads a
+    256 MB buffer before every step (outside the step's own events).  ZeRO-3
+    streams are launched step by step with events per layer (or per pass).
+    Returns the wall-clock window of the timed region and the timings."""
+    import torch
+    Z = run.Z
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        t += 1
+        run.step(t)
+    torch.cuda.synchronize(dev)
+
+    def pair():
+        return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    zero3 = run.w.zero3
+    if zero3:
+        ev = [[pair() for _ in range(1 if run.prefetch else run.layers)] for _ in range(steps)]
+    else:
+        ev = [pair() for _ in range(steps)]
+    graph_obj = None
+    graph_launches = 0
+    use_graph = graph and not flush_l2 and not zero3
+    if use_graph:
+        graph_obj = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        n0 = Z.zero_launch_count()
+        with torch.cuda.graph(graph_obj, stream=cap):
+            for k in range(steps):
+                run.step(t + 1 + k)
+        graph_launches = Z.zero_launch_count() - n0   # kernel nodes the replay runs
+        torch.cuda.synchronize(dev)
+    flush = flush_sink = None
+    if flush_l2:
+        # twice the size of L2, read (not written, which would leave dirty
+        # lines to be written back during the step) before every step
+        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+    barrier(dist, local)
+    torch.cuda.synchronize(dev)
+    launches0 = Z.zero_launch_count()
+    wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    if graph_obj is not None:
+        graph_obj.replay()
+        t += steps
+    else:
+        for k in range(steps):
+            t += 1
+            if flush is not None:
+                torch.sum(flush, dim=0, out=flush_sink)
+            run.step(t, ev[k])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    launches = Z.zero_launch_count() - launches0 + graph_launches
+    barrier(dist, local)
+    elapsed = start.elapsed_time(stop) / 1e3
+    if flush is not None:
+        # the flushes are not part of the step: time the steps by their events
+        elapsed = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    elapsed = max_over_ranks(dist, elapsed, local)
+    if zero3 and run.prefetch:
+        # events bracket whole passes: the pass's bytes (gathers + steps)
+        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
+        bytes_per_launch = run.bytes_per_step
+    elif zero3:
+        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
+        bytes_per_launch = run.kernel_bytes
+    elif graph_obj is not None:
+        kernel_s = elapsed / steps   # graph replay: launches back to back
+        bytes_per_launch = run.bytes_per_step
+    else:
+        kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
+        bytes_per_launch = run.bytes_per_step
+    del graph_obj, flush
+    return {"elapsed": elapsed, "kernel_s": kernel_s, "bytes_per_launch": bytes_per_launch,
+            "launches": launches, "t": t, "use_graph": use_graph, "window": (wall0, wall1)}
+
+
+def regime_text(run, use_graph, flush_l2):
+    if flush_l2:
+        return (f"flushed: a 256 MB buffer is read before every timed step, outside the "
+                f"step's events ({run.bytes_per_step / 1e6:.1f} MB touched per step)")
+    if use_graph:
+        return (f"back to back in a CUDA graph; {run.bytes_per_step / 1e6:.1f} MB touched per "
+                f"step ({'fits' if run.bytes_per_step < 120e6 else 'larger than'} L2)")
+    return f"inputs larger than L2: {run.bytes_per_step / 1e9:.2f} GB touched per step"
+
+
+def per_config(args, dev, clocks, peak):
+    """Every other group of the path, one after another on the same GPU."""
+    import gc
+
+    import torch
+
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    out = {}
+    for key, wkey, regime, opt in PER_CONFIG:
+        if wkey == args.workload and not opt.get("flush_l2"):
+            continue
+        w = W.WORKLOADS[wkey]
+        run = make_runner(w, dev, prefetch=opt.get("prefetch", 0))
+        torch.cuda.synchronize(dev)
+        r = time_steps(run, dev, opt["steps"], opt["warmup"], graph=True,
+                       flush_l2=opt.get("flush_l2", False))
+        sec = r["elapsed"] / opt["steps"]
+        gbs = r["bytes_per_launch"] / r["kernel_s"] / 1e9
+        out[key] = {
+            "workload": w.title, "regime": regime, "steps": opt["steps"],
+            "warmup": opt["warmup"], "ms_per_step": 1e3 * sec,
+            "params_per_s": run.elems / sec, "elements_per_step": run.elems,
+            "bytes_per_step": run.bytes_per_step,
+            "gbs": gbs, "frac": gbs / peak,
+            "kernel": ("zero_zero3_pass (k_allgather + k_step per layer)"
+                       if getattr(run, "prefetch", 0) else run.kernel),
+            "gpu_launches": r["launches"],
+            "clocks": clocks.summary(*r["window"]),
+        }
+        if w.zero3:
+            out[key].update({"layers": run.layers, "layer_states": run.n_states,
+                             "bytes_per_element": 46})
+        del run
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, world, rank, local):
+    import gc
+
     import torch
 
     import zero_sharded_optimizer_flatten_gb300 as Z
@@ -563,98 +743,23 @@ def run_gpu(args, world, rank, local):
     dist = init_dist(world, "nccl")
     w = W.WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
-    if w.zero3:
-        run = Zero3Runner(w, dev, args.layer_states, args.prefetch)
-    else:
-        amp = None
-        if args.amp:
-            amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
-                              max_norm=args.max_norm)
-        run = FlatRunner(w, dev, args.grad_sets, amp, args.offload, args.from_shards)
-    stream = torch.cuda.current_stream(dev)
-    torch.cuda.synchronize(dev)
-
-    t = 0
-    for _ in range(args.warmup):
-        t += 1
-        run.step(t)
+    amp = None
+    if args.amp and not w.zero3:
+        amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
+                          max_norm=args.max_norm)
+    run = make_runner(w, dev, args.grad_sets, amp, args.offload, args.from_shards,
+                      args.layer_states, args.prefetch)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-
-    def pair():
-        return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    if w.zero3:
-        ev = [[pair() for _ in range(1 if run.prefetch else run.layers)]
-              for _ in range(args.steps)]
-    else:
-        ev = [pair() for _ in range(args.steps)]
-    graph = None
-    graph_launches = 0
-    use_graph = args.graph and not args.flush_l2 and not w.zero3
-    if use_graph:
-        # capture the K timed steps (each with its own step number) into one
-        # CUDA graph and replay it once: no host work between the launches
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        n0 = Z.zero_launch_count()
-        with torch.cuda.graph(graph, stream=cap):
-            for k in range(args.steps):
-                run.step(t + 1 + k)
-        graph_launches = Z.zero_launch_count() - n0   # kernel nodes the replay runs
-        torch.cuda.synchronize(dev)
-    flush = None
-    if args.flush_l2:
-        # a buffer twice the size of L2, read (not written, which would leave
-        # dirty lines to be written back during the step) before every step
-        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
-        flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    barrier(dist, local)
-    torch.cuda.synchronize(dev)
-    launches0 = Z.zero_launch_count()
-    wall0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    if graph is not None:
-        graph.replay()
-        t += args.steps
-    else:
-        for k in range(args.steps):
-            t += 1
-            if flush is not None:
-                torch.sum(flush, dim=0, out=flush_sink)
-            run.step(t, ev[k])
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    wall1 = time.time()
-    launches = Z.zero_launch_count() - launches0 + graph_launches
-    barrier(dist, local)
-    clocks.stop()
-    elapsed = start.elapsed_time(stop) / 1e3
-    if flush is not None:
-        # the flushes are not part of the step: time the steps by their events
-        elapsed = sum(a.elapsed_time(b) for a, b in ev) / 1e3
-    elapsed = max_over_ranks(dist, elapsed, local)
-    if w.zero3 and run.prefetch:
-        # events bracket whole passes: report the pass's bytes (gathers + steps)
-        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
-        bytes_per_launch = run.bytes_per_step
-    elif w.zero3:
-        kernel_s = statistics.fmean(a.elapsed_time(b) for st in ev for a, b in st) / 1e3
-        bytes_per_launch = run.kernel_bytes
-    elif graph is not None:
-        kernel_s = elapsed / args.steps   # graph replay: launches back to back
-        bytes_per_launch = run.bytes_per_step
-    else:
-        kernel_s = statistics.fmean(a.elapsed_time(b) for a, b in ev) / 1e3
-        bytes_per_launch = run.bytes_per_step
+    r = time_steps(run, dev, args.steps, args.warmup, args.graph, args.flush_l2, dist, local)
+    elapsed, kernel_s = r["elapsed"], r["kernel_s"]
+    bytes_per_launch, t = r["bytes_per_launch"], r["t"]
 
     e2e = None
-    if not w.zero3 and not args.amp and not args.offload:
+    if not w.zero3 and not args.amp and not args.offload and args.e2e_steps > 0:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         per_step, h2d, d2h = run.e2e(t, e2e_steps)
         link_s = per_step.pop("h2d_only")
@@ -664,9 +769,11 @@ def run_gpu(args, world, rank, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "path": best,
                "ms_per_step": {k: 1e3 * v for k, v in per_step.items()},
-               # the inputs must cross the host link: its copy rate bounds the step
-               "link": {"h2d_gbs": h2d / link_s / 1e9, "h2d_ms": 1e3 * link_s,
-                        "frac": link_s / per_step[best]},
+               # the inputs must cross the host link: the copy engine's rate for
+               # the same replicas (nothing else), next to the rate the direct
+               # path's kernel loads and stores reach across it
+               "link": {"h2d_copy_gbs": h2d / link_s / 1e9, "h2d_copy_ms": 1e3 * link_s,
+                        "direct_gbs": (h2d + d2h) / per_step["direct"] / 1e9},
                "note": "direct: zero_step reads the pinned host replicas and writes the pinned "
                        "host parameters across NVLink-C2C; copies: cudaMemcpyAsync in, "
                        "zero_step, cudaMemcpyAsync out"}
@@ -694,16 +801,10 @@ def run_gpu(args, world, rank, local):
             "virtual_ranks": w.n_ranks,
             "storage": f"{w.dtype} params and gradients, fp32 master/m/v",
             "parallelism": f"{world} independent replica(s); {w.n_ranks} virtual ranks each",
-            "l2": (f"flushed: a 256 MB buffer is read before every timed step, outside "
-                   f"the step's events ({run.bytes_per_step / 1e6:.1f} MB touched per step)"
-                   if args.flush_l2 else
-                   f"back to back in a CUDA graph; {run.bytes_per_step / 1e6:.1f} MB touched "
-                   f"per step ({'fits' if run.bytes_per_step < 120e6 else 'larger than'} L2)"
-                   if use_graph else
-                   f"inputs larger than L2: {run.bytes_per_step / 1e9:.2f} GB touched per step"),
+            "l2": regime_text(run, r["use_graph"], args.flush_l2),
             "hbm_gbs_per_step": run.bytes_per_step / (elapsed / args.steps) / 1e9,
             "launch": ("the K timed steps captured in one CUDA graph (each with its own step "
-                       "number), replayed once" if use_graph else
+                       "number), replayed once" if r["use_graph"] else
                        "one Python call per step through the binding"),
         },
         "roofline": {
@@ -713,16 +814,25 @@ def run_gpu(args, world, rank, local):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": (recorded_traffic(args.workload)
-                        if not (args.amp or args.offload) else None),
+                        if not (args.amp or args.offload or w.zero3) else None),
             "kernel": run.kernel,
             "bytes_per_launch": bytes_per_launch,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                            else "fallback 6.8 TB/s",
         },
         "e2e": e2e,
-        "gpu_launches": launches,
-        "clocks": clocks.summary(wall0, wall1),
+        "gpu_launches": r["launches"],
+        "clocks": clocks.summary(*r["window"]),
     }
+    if w.bucket_elems and not (args.amp or args.offload):
+        # one k_step launch per bucket: the algorithmic bytes of one full
+        # bucket's launch sit beside its measured DRAM traffic; `achieved` is
+        # the step's bytes over the step's time (the launches' average)
+        nb = -(-run.elems // w.bucket_elems)
+        line["roofline"].update({
+            "bytes_per_launch": step_bytes(w.bucket_elems, w.n_ranks),
+            "launches_per_step": nb,
+            "achieved_from": "bytes of the step's launches / their back-to-back time"})
     if args.offload:
         link = 24 * run.elems
         line["config"]["offload"] = {
@@ -745,6 +855,12 @@ def run_gpu(args, world, rank, local):
             line["config"]["prefetch_layer_buffers"] = run.prefetch
         line["config"]["layer_states"] = run.n_states
         line["config"]["layers"] = run.layers
+    del run
+    gc.collect()
+    torch.cuda.empty_cache()
+    if world == 1 and args.per_config and not (args.amp or args.offload):
+        line["per_config"] = per_config(args, dev, clocks, peak)
+    clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     if rank == 0:
@@ -768,7 +884,7 @@ def run_offload_cpu(args, world, rank, local):
     w = W.WORKLOADS[args.workload]
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
     S = [plan.shard_len(r) for r in range(w.n_ranks)]
-    p16 = W.params16(w, dev)
+    p16 = W.params16(w, dev, plan.padded)
     full16 = torch.zeros_like(p16)
     dm = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
     Z.zero_init_shards(plan, p16, dm, [torch.empty_like(x) for x in dm],
@@ -781,7 +897,7 @@ def run_offload_cpu(args, world, rank, local):
     v = [pin(n, torch.float32) for n in S]
     gsh = [pin(n, torch.float32) for n in S]
     s16 = [pin(n, w.torch_dtype) for n in S]
-    grads = [W.grads16(w, 1, q, dev) for q in range(w.n_ranks)]
+    grads = [W.grads16(w, 1, q, dev, 0, plan.padded) for q in range(w.n_ranks)]
     hp = Z.AdamW()
     dt = Z.ZERO_BF16 if w.dtype == "bf16" else Z.ZERO_FP16
     phases = {"reduce": 0.0, "cpu_adamw": 0.0, "gather": 0.0}
@@ -912,7 +1028,7 @@ def run_gather_all(args, world, rank, local):
     if w.mode != "flat":
         raise SystemExit("--gather-all: flat groups only")
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
-    src = W.params16(w, dev)
+    src = W.params16(w, dev, plan.padded)
     shards = [src[off:off + n] for off, n in plan.shards]
     full = torch.zeros_like(src)
     E = plan.padded
@@ -1018,8 +1134,8 @@ def run_engine(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -1027,6 +1143,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the other groups' records (per_config) after the headline")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="parameter group to time (the reported line uses the default)")
     ap.add_argument("--grad-sets", type=int, default=2,

@@ -15,6 +15,12 @@ FP32_RTOL = 1e-6
 ULP16 = 1
 
 
+def flat_len(w: W.Workload) -> int:
+    """Length of the gathered flat buffer (tail padding included), from the
+    oracle's plan."""
+    return oracle.flat_len(list(w.numel), w.n_ranks, mode_code(w), w.align)
+
+
 def dt_code(w: W.Workload) -> int:
     return oracle.FP16 if w.dtype == "fp16" else oracle.BF16
 
@@ -86,9 +92,9 @@ class Case:
     def __init__(self, w: W.Workload, device="cuda", with_oracle=True, layer: int = 0):
         self.w, self.dev = w, device
         self.plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
-        self.L = W.flat_len(w)
+        self.L = flat_len(w)
         assert self.plan.padded == self.L
-        self.p16 = W.params16(w, device, layer=layer)
+        self.p16 = W.params16(w, device, self.L, layer=layer)
         self.full16 = torch.zeros(self.L, dtype=w.torch_dtype, device=device)
         mask = w.mask
         self.master, self.m, self.v = [], [], []
@@ -120,7 +126,7 @@ class Case:
         self.o = True
 
     def grads(self, t: int):
-        return [W.grads16(self.w, t, q, self.dev) for q in range(self.w.n_ranks)]
+        return [W.grads16(self.w, t, q, self.dev, 0, self.L) for q in range(self.w.n_ranks)]
 
     def oracle_step(self, grads, t: int, hp: oracle.Hparams, mask=None):
         w = self.w
@@ -163,7 +169,7 @@ def sample_indices(w: W.Workload, n_random: int = 20000, seed: int = 99, extra=(
     """Seeded random flat indices plus every boundary the kernels care about:
     shard and tensor starts/ends, the tail padding, 2048-element tile edges
     next to shard starts, and caller-given extras (bucket edges)."""
-    L = W.flat_len(w)
+    L = flat_len(w)
     rng = np.random.default_rng(seed)
     # random points inside the flat ranges of the masked ranks only
     ranges = []

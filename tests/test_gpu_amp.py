@@ -55,7 +55,8 @@ class AmpCase(Case):
         self.ost = oracle.amp_init(_ocfg(cfg)) if with_oracle else None
 
     def grads_scaled(self, t, scale):
-        return [W.grads16(self.w, t, q, "cuda", scale=scale) for q in range(self.w.n_ranks)]
+        return [W.grads16(self.w, t, q, "cuda", 0, self.L, scale=scale)
+                for q in range(self.w.n_ranks)]
 
     def gpu_step(self, g):
         Z.zero_step_amp(self.plan, g, self.w.op, self.gsh, self.master, self.m, self.v,

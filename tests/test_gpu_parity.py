@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from tests._harness import (Case, assert_16_close, assert_fp32_close, dt_code, f32,
+from tests._harness import (Case, assert_16_close, assert_fp32_close, dt_code, f32, flat_len,
                             hp_oracle, op_code, owner_of, sample_indices, u16)
 from zero_sharded_optimizer_flatten_gb300 import workloads as W
 from zero_sharded_optimizer_flatten_gb300 import zero as Z
@@ -263,7 +263,7 @@ def _sampled(w: W.Workload, steps: int, hp=HP, n_random=20000, extra=()):
     oracle recomputing those elements one by one from the same inputs."""
     extra = list(extra)
     if w.bucket_elems:
-        extra += list(range(0, W.flat_len(w), w.bucket_elems))
+        extra += list(range(0, flat_len(w), w.bucket_elems))
     F = sample_indices(w, n_random=n_random, extra=extra)
     rank, shard = owner_of(w, F)
     keep = np.array([(w.mask >> int(r)) & 1 for r in rank], bool) & (rank >= 0)
@@ -347,7 +347,7 @@ def test_llama13b_zero3_layer_pass_sampled(key):
     (bit-exact), then the fused step writing each rank's shard."""
     w = W.WORKLOADS[key]
     plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
-    L = W.flat_len(w)
+    L = flat_len(w)
     S = plan.shard_len(0)
     layer_buf = torch.empty(L, dtype=w.torch_dtype, device="cuda")
     F = sample_indices(w, n_random=8000)
@@ -355,7 +355,7 @@ def test_llama13b_zero3_layer_pass_sampled(key):
     Ft = torch.from_numpy(F).cuda()
     dt, op = dt_code(w), op_code(w)
     for layer in range(2):
-        p16 = W.params16(w, "cuda", layer=layer)
+        p16 = W.params16(w, "cuda", L, layer=layer)
         shards = [p16[r * S:(r + 1) * S].clone() for r in range(w.n_ranks)]
         master = [torch.empty(S, dtype=torch.float32, device="cuda") for _ in range(w.n_ranks)]
         m = [torch.empty_like(x) for x in master]
@@ -367,7 +367,7 @@ def test_llama13b_zero3_layer_pass_sampled(key):
         om = oracle.to_f32(u16(p16[Ft]), dt)
         mm, vv = np.zeros_like(om), np.zeros_like(om)
         out = np.zeros(F.size, np.uint16)
-        g = [W.grads16(w, 1, q, "cuda", layer=layer) for q in range(w.n_ranks)]
+        g = [W.grads16(w, 1, q, "cuda", 0, L, layer=layer) for q in range(w.n_ranks)]
         gs = np.stack([u16(x[Ft]) for x in g])
         Z.zero_step(plan, g, "avg", master, m, v, None, shards, HP, 1)
         oracle.update_elements(gs, om, mm, vv, dt, op, hp_oracle(HP), 1, out16=out)
@@ -413,7 +413,7 @@ def test_optimizer_state_in_host_memory():
     gradients and parameters in HBM; bit-identical to device-resident state,
     through init, the fused step and the unfused pieces."""
     w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
-    dev_case = Case(w, with_oracle=False)
+    dev_case = Case(w)
     plan = dev_case.plan
     S = [plan.shard_len(r) for r in range(4)]
     hm = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in S]
@@ -426,11 +426,17 @@ def test_optimizer_state_in_host_memory():
         Z.zero_step(plan, g, "avg", dev_case.master, dev_case.m, dev_case.v, dev_case.full16, None,
                     HP, t)
         Z.zero_step(plan, g, "avg", hm, hmm, hv, full, None, HP, t)
+        dev_case.oracle_step(g, t, hp_oracle(HP))
     torch.cuda.synchronize()
     for r in range(4):
         assert torch.equal(dev_case.master[r].cpu(), hm[r])
         assert torch.equal(dev_case.m[r].cpu(), hmm[r]) and torch.equal(dev_case.v[r].cpu(), hv[r])
+        # the host-resident state against the oracle
+        assert_fp32_close(hm[r].numpy(), dev_case.o_master[r], f"host master[{r}]")
+        assert_fp32_close(hmm[r].numpy(), dev_case.o_m[r], f"host m[{r}]")
+        assert_fp32_close(hv[r].numpy(), dev_case.o_v[r], f"host v[{r}]")
     assert torch.equal(dev_case.full16, full)
+    assert_16_close(u16(full), dev_case.o_full, "full16", dtype_code=dt_code(w))
 
 
 def test_cpu_optimizer_offload_pipeline():
@@ -438,7 +444,7 @@ def test_cpu_optimizer_offload_pipeline():
     host fp32 shards, host threads run AdamW on host-resident state, the GPU
     all-gathers the host 16-bit shards.  Bit-identical to the fused step."""
     w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
-    dev_case = Case(w, with_oracle=False)
+    dev_case = Case(w)
     plan = dev_case.plan
     S = [plan.shard_len(r) for r in range(4)]
     pin = lambda n, dt: torch.zeros(n, dtype=dt, pin_memory=True)  # noqa: E731
@@ -456,11 +462,20 @@ def test_cpu_optimizer_offload_pipeline():
         Z.zero_sync()
         Z.zero_cpu_adamw_shard_step(plan, hm, hmm, hv, hg, h16, HP, t, Z.ZERO_BF16)
         Z.zero_allgather(plan, h16, full)
+        dev_case.oracle_step(g, t, hp_oracle(HP))
     torch.cuda.synchronize()
     for r in range(4):
         assert torch.equal(dev_case.master[r].cpu(), hm[r])
         assert torch.equal(dev_case.v[r].cpu(), hv[r])
+        # the host optimizer's state and 16-bit shards against the oracle
+        assert_fp32_close(hm[r].numpy(), dev_case.o_master[r], f"host master[{r}]")
+        assert_fp32_close(hmm[r].numpy(), dev_case.o_m[r], f"host m[{r}]")
+        assert_fp32_close(hv[r].numpy(), dev_case.o_v[r], f"host v[{r}]")
+        off = int(dev_case.o_seg[r][0, 2])          # flat offset of the shard (oracle plan)
+        assert_16_close(u16(h16[r]), dev_case.o_full[off:off + S[r]], f"host shard16[{r}]",
+                        dtype_code=dt_code(w))
     assert torch.equal(dev_case.full16, full)
+    assert_16_close(u16(full), dev_case.o_full, "full16", dtype_code=dt_code(w))
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])

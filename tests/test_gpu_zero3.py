@@ -1,11 +1,16 @@
 """The ZeRO-3 layer stream (zero_zero3_pass): gathers on one stream run ahead
-of the fused steps on another; results must equal the serial pass of the
-already-tested pieces (zero_allgather then zero_step, layer by layer)."""
+of the fused steps on another.  Results must equal the oracle's layer pass
+(per layer: gather the 16-bit shards into the layer buffer, then the step
+writing each rank's shard) and the serial pass of the already-tested pieces
+(zero_allgather then zero_step, layer by layer)."""
 import gc
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
+from tests._harness import assert_16_close, assert_fp32_close, f32, hp_oracle, u16
 from zero_sharded_optimizer_flatten_gb300 import workloads as W
 from zero_sharded_optimizer_flatten_gb300 import zero as Z
 
@@ -27,48 +32,92 @@ def _cuda_cleanup():
 def _layers(w, plan, n_layers):
     out = []
     for layer in range(n_layers):
-        p16 = W.params16(w, "cuda", layer=layer)
+        p16 = W.params16(w, "cuda", plan.padded, layer=layer)
         off = [plan.shards[r][0] for r in range(w.n_ranks)]
         S = [plan.shard_len(r) for r in range(w.n_ranks)]
-        L = {"grads": [W.grads16(w, 1, q, "cuda", layer=layer) for q in range(w.n_ranks)],
+        L = {"grads": [W.grads16(w, 1, q, "cuda", 0, plan.padded, layer=layer)
+                       for q in range(w.n_ranks)],
              "shards16": [p16[off[r]:off[r] + S[r]].clone() for r in range(w.n_ranks)],
              "master": [torch.empty(n, dtype=torch.float32, device="cuda") for n in S]}
         L["m"] = [torch.empty_like(x) for x in L["master"]]
         L["v"] = [torch.empty_like(x) for x in L["master"]]
         Z.zero_init_shards(plan, p16, L["master"], L["m"], L["v"])
+        L["p16"] = u16(p16)
         out.append(L)
     return out
 
 
+def _oracle_layer(w, L):
+    """The oracle's copy of one layer: master = the 16-bit partition widened,
+    m = v = 0, the 16-bit shards and the gradient replicas as drawn."""
+    o = {"master": [], "m": [], "v": [], "shards16": [u16(x) for x in L["shards16"]],
+         "grads": [u16(x) for x in L["grads"]]}
+    for r in range(w.n_ranks):
+        seg = oracle.segments(list(w.numel), w.n_ranks, oracle.FLAT, w.align, r)
+        S = int(seg[:, 4].sum()) if len(seg) else 0
+        mst = np.zeros(S, np.float32)
+        for k, toff, foff, soff, ln in seg:
+            mst[soff:soff + ln] = oracle.to_f32(L["p16"][foff:foff + ln], oracle.BF16)
+        o["master"].append(mst)
+        o["m"].append(np.zeros(S, np.float32))
+        o["v"].append(np.zeros(S, np.float32))
+    return o
+
+
 @pytest.mark.parametrize("n_bufs,two_streams", [(1, False), (1, True), (2, True), (3, True)])
-def test_zero3_pass_equals_serial_pieces(n_bufs, two_streams):
+def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams):
     w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
     plan = Z.zero_plan_partitions(list(w.numel), 4, "flat", 16)
     n_layers = 5
     ref = _layers(w, plan, n_layers)
     got = _layers(w, plan, n_layers)
+    orc = [_oracle_layer(w, L) for L in got]
+    o_bufs = [np.zeros(plan.padded, np.uint16) for _ in range(n_layers)]
     ref_bufs = [torch.empty(plan.padded, dtype=w.torch_dtype, device="cuda")
                 for _ in range(n_layers)]
     bufs = [torch.full((plan.padded,), 3.0, dtype=w.torch_dtype, device="cuda")
             for _ in range(n_bufs)]
     gather = torch.cuda.Stream() if two_streams else None
     passer = Z.Zero3Pass(plan, got, bufs, "avg", HP)
+    hp = hp_oracle(HP)
+    after_step1 = None
     for t in (1, 2):
         for layer in range(n_layers):
             L = ref[layer]
             Z.zero_allgather(plan, L["shards16"], ref_bufs[layer])
             Z.zero_step(plan, L["grads"], "avg", L["master"], L["m"], L["v"], None,
                         L["shards16"], HP, t)
+            # the oracle's layer pass: gather, then the step writing the shards
+            o = orc[layer]
+            oracle.allgather(list(w.numel), 4, oracle.FLAT, 16, o["shards16"], o_bufs[layer])
+            oracle.step(list(w.numel), 4, oracle.FLAT, 16, oracle.BF16, oracle.AVG, o["grads"],
+                        o["master"], o["m"], o["v"], None, o["shards16"], hp, t)
         passer(t, gather_stream=gather)
+        if t == 1:
+            torch.cuda.synchronize()
+            after_step1 = [[u16(x) for x in L["shards16"]] for L in got]
     torch.cuda.synchronize()
     for layer in range(n_layers):
+        o = orc[layer]
         for r in range(4):
             for key in ("master", "m", "v", "shards16"):
                 assert torch.equal(got[layer][key][r], ref[layer][key][r]), (layer, key, r)
-    # each buffer holds the last gather that used it (of step 2)
+            what = f"layer {layer} rank {r}"
+            assert_fp32_close(f32(got[layer]["master"][r]), o["master"][r], what + " master")
+            assert_fp32_close(f32(got[layer]["m"][r]), o["m"][r], what + " m")
+            assert_fp32_close(f32(got[layer]["v"][r]), o["v"][r], what + " v")
+            assert_16_close(u16(got[layer]["shards16"][r]), o["shards16"][r], what + " shard16",
+                            dtype_code=oracle.BF16)
+    # each buffer holds the last gather that used it (of step 2): the oracle's
+    # gather of the shards the pass wrote at step 1, bit for bit, and the
+    # oracle's own layer buffer within the 16-bit bar
     for b in range(n_bufs):
         last = max(l for l in range(n_layers) if l % n_bufs == b)
         assert torch.equal(bufs[b], ref_bufs[last])
+        want = np.zeros(plan.padded, np.uint16)
+        oracle.allgather(list(w.numel), 4, oracle.FLAT, 16, after_step1[last], want)
+        assert np.array_equal(u16(bufs[b]), want), f"buffer {b}"
+        assert_16_close(u16(bufs[b]), o_bufs[last], f"buffer {b}", dtype_code=oracle.BF16)
 
 
 def test_zero3_pass_rejects_a_bad_layer_before_launching():

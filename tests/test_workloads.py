@@ -10,8 +10,8 @@ from zero_sharded_optimizer_flatten_gb300 import workloads as W
 def test_subranges_match_the_whole_draw():
     w = W.small((W.CHUNK + 1234, 77, 3 * W.CHUNK // 2), 3, mode="flat", align=16, dtype="bf16",
                 outlier_frac=0.01)
-    L = W.flat_len(w)
-    whole = W.grads16(w, 2, 1, "cpu")
+    L = w.phi + 50                    # a buffer with 50 elements of tail padding
+    whole = W.grads16(w, 2, 1, "cpu", 0, L)
     rng = np.random.default_rng(0)
     for _ in range(8):
         lo = int(rng.integers(0, L - 1))
@@ -23,19 +23,22 @@ def test_subranges_match_the_whole_draw():
 
 def test_draws_depend_on_step_rank_layer_kind():
     w = W.small((5000,), 2, dtype="fp16")
-    a = W.grads16(w, 1, 0, "cpu")
-    assert not torch.equal(a, W.grads16(w, 2, 0, "cpu"))
-    assert not torch.equal(a, W.grads16(w, 1, 1, "cpu"))
-    assert not torch.equal(a, W.grads16(w, 1, 0, "cpu", layer=1))
-    assert not torch.equal(W.params16(w, "cpu"), W.params16(w, "cpu", layer=1))
-    assert torch.equal(a, W.grads16(w, 1, 0, "cpu"))              # reproducible
+    n = w.phi
+    a = W.grads16(w, 1, 0, "cpu", 0, n)
+    assert not torch.equal(a, W.grads16(w, 2, 0, "cpu", 0, n))
+    assert not torch.equal(a, W.grads16(w, 1, 1, "cpu", 0, n))
+    assert not torch.equal(a, W.grads16(w, 1, 0, "cpu", 0, n, layer=1))
+    assert not torch.equal(W.params16(w, "cpu", n), W.params16(w, "cpu", n, layer=1))
+    assert torch.equal(a, W.grads16(w, 1, 0, "cpu", 0, n))        # reproducible
 
 
 def test_scale_multiplies_before_rounding():
     w = W.small((5000,), 1, dtype="fp16", grad_sigma=1.0)
-    big = W.grads16(w, 1, 0, "cpu", scale=1e5).float()
+    n = w.phi
+    big = W.grads16(w, 1, 0, "cpu", 0, n, scale=1e5).float()
     assert torch.isinf(big).any()                               # fp16 overflow appears
-    assert torch.equal(W.grads16(w, 1, 0, "cpu", scale=1.0), W.grads16(w, 1, 0, "cpu"))
+    assert torch.equal(W.grads16(w, 1, 0, "cpu", 0, n, scale=1.0),
+                       W.grads16(w, 1, 0, "cpu", 0, n))
 
 
 def test_group_sizes():

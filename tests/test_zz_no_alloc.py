@@ -54,7 +54,7 @@ def test_noalloc_matches_workspace_entry_point(numel, N, mode, dtype, op, cfg):
     ws = torch.empty(Z.zero_amp_workspace_bytes(ref.plan), dtype=torch.uint8, device="cuda")
     for t in (1, 2):   # two calls in a row on the same fixed scratch
         scale = Z.read_amp_state(ref.state).scale
-        g = [W.grads16(w, t, q, "cuda", scale=scale) for q in range(N)]
+        g = [W.grads16(w, t, q, "cuda", 0, ref.L, scale=scale) for q in range(N)]
         Z.zero_step_amp(ref.plan, g, op, ref.gsh, ref.master, ref.m, ref.v, ref.full16, None, HP,
                         cfg, ref.state, ws)
         Z.zero_step_amp_noalloc(got.plan, g, op, got.gsh, got.master, got.m, got.v, got.full16,

@@ -147,14 +147,6 @@ WORKLOADS = {
 }
 
 
-def flat_len(w: Workload) -> int:
-    """Length of the gathered flat buffer (tail padding included)."""
-    if w.mode == "round_robin":
-        return w.phi
-    unit = w.n_ranks * w.align
-    return -(-w.phi // unit) * unit
-
-
 def _seed(*parts) -> int:
     h = hashlib.blake2b(repr(parts).encode(), digest_size=8).digest()
     return int.from_bytes(h, "little") & ((1 << 63) - 1)
@@ -202,14 +194,15 @@ def fill(w: Workload, kind: str, step: int, rank: int, lo: int, hi: int, out: to
     return out
 
 
-def params16(w: Workload, device, layer: int = 0) -> torch.Tensor:
-    n = flat_len(w)
+def params16(w: Workload, device, n: int, layer: int = 0) -> torch.Tensor:
+    """The initial 16-bit parameters of flat range [0, n); n is the flat
+    buffer length the caller's plan gives (tail padding included)."""
     return fill(w, "param", 0, 0, 0, n, torch.empty(n, dtype=w.torch_dtype, device=device), layer)
 
 
-def grads16(w: Workload, step: int, rank: int, device, lo: int = 0, hi: Optional[int] = None,
-            layer: int = 0, scale: float = 1.0) -> torch.Tensor:
-    hi = flat_len(w) if hi is None else hi
+def grads16(w: Workload, step: int, rank: int, device, lo: int, hi: int, layer: int = 0,
+            scale: float = 1.0) -> torch.Tensor:
+    """Rank `rank`'s gradient replica at `step` over flat range [lo, hi)."""
     return fill(w, "grad", step, rank, lo, hi,
                 torch.empty(hi - lo, dtype=w.torch_dtype, device=device), layer, scale)
 
