@@ -416,7 +416,13 @@ zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dtype,
  *    ZERO_ERR_INVALID and a message, and nothing is launched;
  *  - the first call on a device looks up the array's device address with
  *    that device current and caches it; make that first call before any
- *    stream capture begins;
+ *    stream capture begins.  With CUDA's lazy module loading (the default)
+ *    that lookup is also what loads the library's device code on that
+ *    device and commits the 2 MiB array, so the first call can fail with
+ *    ZERO_ERR_CUDA (out of memory) on a device that is already full; later
+ *    calls commit nothing;
+ *  - the cached address belongs to the device's current context: do not call
+ *    cudaDeviceReset on that device between calls of this function;
  *  - every call on a device shares the one array, which keeps what the last
  *    call left there (each call writes everything it reads, so nothing needs
  *    clearing): calls whose work overlaps on the GPU (different streams,

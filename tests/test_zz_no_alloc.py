@@ -90,3 +90,30 @@ def test_noalloc_rejects_steps_beyond_the_fixed_scratch():
     assert e.value.status == Z.ZERO_ERR_INVALID
     assert "fixed scratch" in str(e.value) and "zero_step_amp" in str(e.value)
     assert Z.zero_launch_count() == before
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """After a first call (which may load the library's device code on this
+    device and commit the fixed scratch), further calls leave the device's
+    free memory and torch's allocation counters unchanged."""
+    w = W.small((20000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+    cfg = Z.AmpConfig(init_scale=1.0, window=0, hysteresis=1, max_norm=1.0)
+    c = _setup(w, cfg)
+    g = [W.grads16(w, 1, q, "cuda", 0, c.L) for q in range(4)]
+
+    def call():
+        Z.zero_step_amp_noalloc(c.plan, g, "avg", c.gsh, c.master, c.m, c.v, c.full16, None, HP,
+                                cfg, c.state)
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0
+    for k in ("allocation.all.allocated", "segment.all.allocated", "num_alloc_retries"):
+        assert stats1.get(k, 0) == stats0.get(k, 0), k
+    assert Z.read_amp_state(c.state).step == 4

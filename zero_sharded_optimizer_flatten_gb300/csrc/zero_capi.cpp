@@ -143,6 +143,9 @@ void build_jobs(const zero_plan* plan, uint64_t mask, int64_t lo, int64_t hi,
 // Launch `kind` over `jobs`, at most kMaxJobs per launch.  `tiles_done`
 // (nullable) numbers the tiles across launches: each launch's first tile is
 // given index *tiles_done (LaunchArgs::tile_base), which then advances.
+// The first launch is ordered after everything before it on the stream when
+// a.early is 0 on entry; every later one is launched early (its jobs are
+// disjoint from the ones before it; see grid_dependency_begin).
 zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs& a,
                         const std::vector<Job>& jobs, void* stream, int64_t* tiles_done) {
   size_t j0 = 0;
@@ -162,6 +165,7 @@ zero_status launch_jobs(const char* fn, Kind kind, zero_dtype dtype, LaunchArgs&
       return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                   cudaGetErrorString(static_cast<cudaError_t>(err)));
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    a.early = 1;  // the next launch of this run touches other elements
     if (tiles_done) *tiles_done += tiles;
     j0 += nj;
   }
@@ -179,6 +183,7 @@ zero_status run_buckets(const char* fn, Kind kind, zero_dtype dtype, const zero_
                         uint64_t mask, int64_t bucket, LaunchArgs& a, void* stream,
                         int64_t* tiles_done = nullptr) {
   set_bounds(a, plan);
+  a.early = 0;  // the run's first launch waits for all earlier work on the stream
   std::vector<Job> jobs;
   const int64_t total = plan->padded;
   const int64_t B = bucket > 0 ? bucket : std::max<int64_t>(total, 1);
@@ -327,6 +332,7 @@ extern "C" zero_status zero_reduce_scatter_range(const zero_plan* plan, const vo
   std::vector<Job> jobs;
   build_jobs(plan, rank_mask, flat_lo, flat_hi, jobs);
   if (jobs.empty()) return ZERO_OK;
+  a.early = 0;
   return launch_jobs(fn, Kind::kReduceScatter, dtype, a, jobs, stream, nullptr);
 }
 
@@ -590,6 +596,7 @@ zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* g
     a.n_jobs = 0;
     a.n_tiles = 0;
     a.tile_base = 0;
+    a.early = 0;
     const int err = launch_kernel(stats, dtype, a, stream);
     if (err != 0)
       return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,

@@ -21,17 +21,6 @@ constexpr int kHalf = kThreads * kVec;  // 1024: distance between a thread's two
 constexpr int kTile = 2 * kHalf;  // 2048 elements per CTA per tile
 constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 
-// Fused step through bulk-copy (TMA) staging: 0 never; 1 whenever every job
-// of the launch has 8-element-aligned offsets and length; 2 only for launches
-// of at most ZERO_TMA_MAX_TILES tiles (small groups, which one wave of the
-// plain kernel cannot pipeline).
-#ifndef ZERO_STEP_TMA
-#define ZERO_STEP_TMA 0
-#endif
-#ifndef ZERO_TMA_MAX_TILES
-#define ZERO_TMA_MAX_TILES 4096
-#endif
-
 // Resident CTAs per SM the kernels are compiled for (caps registers at 64),
 // and the grid: ZERO_GRID_MULT = 0 launches one CTA per tile; k > 0 caps the
 // grid at k times the resident capacity (the CTAs then stride over tiles).
@@ -53,24 +42,12 @@ constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
 #endif
 constexpr int kGatherTiles = ZERO_GATHER_TILES;
 
-// Programmatic dependent launch (tuning switch): every kernel is launched
-// with the programmatic-stream-serialization attribute, waits for the grid
-// before it (griddepcontrol.wait) before touching global memory, and then
-// lets the grid after it launch (griddepcontrol.launch_dependents), so a
-// launch overlaps the tail of its predecessor instead of following it.
-#ifndef ZERO_PDL
-#define ZERO_PDL 0
-#endif
-
-// Consecutive 2048-element tiles one CTA of the shard-only sum of squares
-// (k_shard_stats) reads.  Measured on the BERT-base group (mixed-precision
-// step from reduced shards): 1 / 2 / 4 / 8 tiles 613 / 598 / 602 / 657 us
-// per step; a persistent grid that prefetches the next two tiles while
-// reducing the current ones took 160 us per launch against 127 us for 2.
-#ifndef ZERO_SHARD_STATS_TILES
-#define ZERO_SHARD_STATS_TILES 2
-#endif
-constexpr int kShardStatsTiles = ZERO_SHARD_STATS_TILES;
+// The shard-only sum of squares (k_shard_stats) gives a 2048-element tile to
+// kShardStatsThreads threads, each holding four of the tile's 256 slots, so
+// a CTA takes kShardStatsTiles consecutive tiles.
+constexpr int kShardStatsThreads = 64;
+constexpr int kShardStatsTiles = kThreads / kShardStatsThreads;
+static_assert(kTile / kVec / 2 == 4 * kShardStatsThreads, "four slots per thread");
 
 // Bounds-checked build: every kernel access is checked against the plan's
 // buffer lengths; a violation skips the access and sets the device error
@@ -128,7 +105,7 @@ struct LaunchArgs {
   int32_t scale_mode;
   int32_t n_ranks;                 // gradient replicas summed
   int32_t n_jobs;
-  int32_t pad_;
+  int32_t early;                   // launched early: wait for the previous launch at the end
   int64_t n_tiles;
   struct NormPartial* partials;    // mixed-precision: per-tile sums of squares
   int64_t tile_base;               // index of this launch's first tile among the step's

@@ -242,22 +242,33 @@ __device__ __forceinline__ void store_16x2(void* base, int64_t i0, int64_t i1, b
 // ---------------------------------------------------------------------------
 // launch ordering
 
-// First statement of every kernel: with ZERO_PDL, wait until the preceding
-// grid on the stream has completed and its writes are visible, then allow
-// the next grid to launch.  Without it (or without the launch attribute)
-// stream order alone separates the kernels.
+// Launches of one call that touch disjoint elements (the buckets of a step,
+// or the several launches of a bucket that holds more than kMaxJobs jobs)
+// need not wait for one another.  Every launch of a call but the first is
+// made with the programmatic-stream-serialization attribute, and every
+// kernel lets its successor launch as soon as all its CTAs have started
+// (griddepcontrol.launch_dependents), so the next launch's CTAs fill the
+// SMs that the current launch's last wave leaves idle.  A kernel launched
+// that way does its own work at once and, as its last action, waits for the
+// launch before it to complete (griddepcontrol.wait).  So no launch of the
+// call completes before the ones ahead of it, and the next call's first
+// launch, made without the attribute, still starts only after all of them.
+// The wait ends: the launch before has no CTA left to schedule (all of them
+// started before this launch could begin) and waits on nothing itself but
+// its own predecessor.
 __device__ __forceinline__ void grid_dependency_begin() {
-#if ZERO_PDL
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-#endif
 }
 
-// Host: launch `fn` on `s`, with the programmatic-serialization attribute
-// when ZERO_PDL is set.
+__device__ __forceinline__ void grid_dependency_end(const LaunchArgs& a) {
+  if (a.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Host: launch `fn` on `s`; early != 0 adds the programmatic-stream-
+// serialization attribute (see grid_dependency_begin).
 inline cudaError_t launch_ordered(const void* fn, dim3 grid, dim3 block, void** args,
-                                  size_t smem, cudaStream_t s) {
-#if ZERO_PDL
+                                  size_t smem, cudaStream_t s, bool early) {
+  if (!early) return cudaLaunchKernel(fn, grid, block, args, smem, s);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -269,9 +280,6 @@ inline cudaError_t launch_ordered(const void* fn, dim3 grid, dim3 block, void** 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
-#else
-  return cudaLaunchKernel(fn, grid, block, args, smem, s);
-#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -369,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_step(const __grid
         if (a.full16) static_cast<uint16_t*>(a.full16)[f] = o;
         if (a.shard16[r]) static_cast<uint16_t*>(a.shard16[r])[i] = o;
       });
+  grid_dependency_end(a);
 }
 
 // Reduce-scatter alone: fp32 gradient shards.
@@ -386,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_reduce_scatter(co
       [&](const Job& jb, int64_t e) {
         a.gshard[jb.rank][jb.shard_off + e] = reduce1<T, NR>(a, jb.flat_off + e);
       });
+  grid_dependency_end(a);
 }
 
 // AdamW + cast on fp32 gradient shards.
@@ -419,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw(const __gri
         a.v[r][i] = v;
         if (a.shard16[r]) static_cast<uint16_t*>(a.shard16[r])[i] = Fmt<T>::narrow(p);
       });
+  grid_dependency_end(a);
 }
 
 // All-gather: copy each rank's 16-bit shard into the flat buffer.  A copy
@@ -474,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_allgather(const _
       }
     }
   }
+  grid_dependency_end(a);
 }
 
 // Initialise a rank's fp32 master from its 16-bit partition; zero m and v.
@@ -502,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_init(const __grid
         a.m[r][i] = 0.f;
         a.v[r][i] = 0.f;
       });
+  grid_dependency_end(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -699,74 +712,122 @@ template <class T, int NR>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_stats(const __grid_constant__ LaunchArgs a) {
   grid_dependency_begin();
   stats_tiles<T, NR>(a);
+  grid_dependency_end(a);
 }
 
 // Per-tile sums of squares of gradients already reduced into the fp32
-// shards (one 4-byte read per element).  Reading 8 KB per tile is too little
-// to amortise a CTA, so a CTA takes kShardStatsTiles consecutive tiles: every
-// load first, then each tile's sum in the same order as stats_tiles (a
-// thread's elements in order, the warp's shuffle tree, the warps in index
-// order), so the partials are bit-identical to those of k_stats on the same
-// tiles.
+// shards (one 4-byte read per element), bit-identical to the partials of
+// k_stats on the same tiles.  k_stats sums a tile as 256 "slots" (a
+// thread's eight elements, added in a fixed order), then the warp's shuffle
+// tree over its 32 slots (slot i + 16 into slot i, then i + 8, 4, 2, 1),
+// then the 8 warps' sums in index order.  Here 64 threads take a tile: the
+// thread with index i in its group g of 8 holds slots 32g + i + 8k
+// (k = 0..3), so the first two levels of the tree are additions inside the
+// thread and only the last three cross threads (shuffles within the group
+// of 8); the tree and the per-tile overhead then cost a quarter of what one
+// slot per thread costs.  A CTA of kThreads threads takes kShardStatsTiles
+// consecutive tiles.
 template <class T>
 __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_shard_stats(const __grid_constant__ LaunchArgs a) {
   grid_dependency_begin();
   constexpr int K = kShardStatsTiles;
-  __shared__ SqSum warp_part[K][kThreads / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kGroups = kShardStatsThreads / 8;  // = the warps of a k_stats tile
+  static_assert(kGroups == kThreads / 32, "one group of 8 threads per k_stats warp");
+  __shared__ SqSum grp_part[K][kGroups];
+  const int sub = threadIdx.x / kShardStatsThreads;            // the CTA's tile
+  const int u = threadIdx.x % kShardStatsThreads;
+  const int grp = u >> 3, i = u & 7;
   for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * K; t0 < a.n_tiles;
        t0 += static_cast<int64_t>(gridDim.x) * K) {
-    int job[K];
-    bool quads[K];
-    float g[K][8];
+    const int64_t tile = t0 + sub;
+    SqSum s[4];
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int64_t tile = t0 + k;
-      job[k] = tile < a.n_tiles ? find_job(a, tile) : -1;
-      quads[k] = false;
-      if (job[k] < 0) continue;
-      const Job& jb = a.jobs[job[k]];
-      if (!jb.vec) continue;
-      const int64_t e0 = (tile - jb.tile_begin) * kTile + static_cast<int64_t>(threadIdx.x) * kVec;
-      const bool two = e0 + kHalf < jb.len;
-      if (e0 < jb.len && access_ok(a, jb, e0, kVec) && (!two || access_ok(a, jb, e0 + kHalf, kVec))) {
-        const int64_t i0 = jb.shard_off + e0;
-        load_state2(a.gshard[jb.rank], i0, i0 + kHalf, two, g[k]);
-        quads[k] = true;
-      }
-    }
+    for (int k = 0; k < 4; ++k) s[k] = sq_zero();
+    if (tile < a.n_tiles) {
+      const Job& jb = a.jobs[find_job(a, tile)];
+      const int64_t base = (tile - jb.tile_begin) * kTile;
+      const float* src = a.gshard[jb.rank] + jb.shard_off;
+      if (jb.vec) {
+        float g[4][8];
+        bool live[4];
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      SqSum s = sq_zero();
-      if (job[k] >= 0) {
-        const Job& jb = a.jobs[job[k]];
-        if (quads[k]) {
+        for (int k = 0; k < 4; ++k) {  // every load first
+          const int64_t e0 = base + static_cast<int64_t>(32 * grp + i + 8 * k) * kVec;
+          const bool two = e0 + kHalf < jb.len;
+          live[k] = e0 < jb.len && access_ok(a, jb, e0, kVec) &&
+                    (!two || access_ok(a, jb, e0 + kHalf, kVec));
 #pragma unroll
-          for (int e = 0; e < 8; ++e) s.add(__fmul_rn(g[k][e], g[k][e]));
-        } else if (!jb.vec) {
-          const int64_t base = (t0 + k - jb.tile_begin) * kTile;
+          for (int e = 0; e < 8; ++e) g[k][e] = 0.f;
+          if (live[k]) load_state2(src, e0, e0 + kHalf, two, g[k]);
+        }
+        // For a binary32 g, g*g < 2^64 exactly when |g| < 2^32 (bit pattern
+        // below 0x4f800000; NaN and infinity are above it).  When that holds
+        // for all 32 values, every square goes to the low range and the
+        // per-element range test can go: the same additions in the same
+        // order as SqSum::add, so the partials do not change.
+        uint32_t top = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) top = max(top, __float_as_uint(g[k][e]) & 0x7fffffffu);
+        if (top < 0x4f800000u) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (live[k]) s[k].a = pair_add1(s[k].a, __fmul_rn(g[k][e], g[k][e]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (live[k]) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) s[k].add(__fmul_rn(g[k][e], g[k][e]));
+            }
+        }
+      } else {
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          const int64_t slot = 32 * grp + i + 8 * k;
 #pragma unroll 1
           for (int e = 0; e < kTile / kThreads; ++e) {
-            const int64_t x = base + e * kThreads + threadIdx.x;
+            const int64_t x = base + e * kThreads + slot;
             if (x < jb.len && access_ok(a, jb, x, 1)) {
-              const float v = a.gshard[jb.rank][jb.shard_off + x];
-              s.add(__fmul_rn(v, v));
+              const float v = src[x];
+              s[k].add(__fmul_rn(v, v));
             }
           }
         }
       }
-      s = warp_sum(s);
-      if (lane == 0) warp_part[k][warp] = s;
     }
+    // the tree: slot i + 16 into i and i + 24 into i + 8, then i + 8 into
+    // i (inside the thread), then 4, 2, 1 across the group
+    SqSum c;
+    c.a = pair_add(pair_add(s[0].a, s[2].a), pair_add(s[1].a, s[3].a));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1)
+      c.a = pair_add(c.a, Pair{__shfl_down_sync(0xffffffffu, c.a.hi, o, 8),
+                               __shfl_down_sync(0xffffffffu, c.a.lo, o, 8)});
+    c.b = s[0].b;
+    const bool big = s[0].b.hi != 0.f || s[1].b.hi != 0.f || s[2].b.hi != 0.f ||
+                     s[3].b.hi != 0.f;
+    if (__any_sync(0xffffffffu, big)) {  // squares >= 2^64 somewhere in the warp
+      c.b = pair_add(pair_add(s[0].b, s[2].b), pair_add(s[1].b, s[3].b));
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1)
+        c.b = pair_add(c.b, Pair{__shfl_down_sync(0xffffffffu, c.b.hi, o, 8),
+                                 __shfl_down_sync(0xffffffffu, c.b.lo, o, 8)});
+    }
+    if (i == 0) grp_part[sub][grp] = c;
     __syncthreads();
     if (threadIdx.x < K && t0 + threadIdx.x < a.n_tiles) {
-      SqSum t = warp_part[threadIdx.x][0];
-      for (int w = 1; w < kThreads / 32; ++w) t.add(warp_part[threadIdx.x][w]);
+      SqSum t = grp_part[threadIdx.x][0];
+      for (int w = 1; w < kGroups; ++w) t.add(grp_part[threadIdx.x][w]);
       store_partial(a.partials + a.tile_base + t0 + threadIdx.x, t);
     }
     __syncthreads();
   }
   prepare_decision(a);
+  grid_dependency_end(a);
 }
 
 // AdamW + cast + all-gather on the reduced fp32 gradient times the decision
@@ -780,7 +841,10 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw_amp(const _
                               threadIdx.x);
   __syncthreads();
   const AmpBcast& d = *reinterpret_cast<const AmpBcast*>(rec);
-  if (d.overflow != 0) return;
+  if (d.overflow != 0) {
+    grid_dependency_end(a);
+    return;
+  }
   const float coef = d.coef;
   StepScalars sc;
   sc.d = d.sc[0];
@@ -822,6 +886,7 @@ __global__ void __launch_bounds__(kThreads, ZERO_MIN_BLOCKS) k_adamw_amp(const _
         if (a.full16) static_cast<uint16_t*>(a.full16)[f] = o;
         if (a.shard16[r]) static_cast<uint16_t*>(a.shard16[r])[i] = o;
       });
+  grid_dependency_end(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -861,20 +926,8 @@ struct PickStats {
 };
 
 template <class T>
-int launch_step_tma(const LaunchArgs& a, cudaStream_t s);
-
-template <class T>
 int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
   const void* fn = nullptr;
-  if (kind == Kind::kStep && ZERO_STEP_TMA != 0 && a.n_ranks >= 1 && a.n_ranks <= 8 &&
-      (ZERO_STEP_TMA == 1 || a.n_tiles <= ZERO_TMA_MAX_TILES)) {
-    bool eligible = true;
-    for (int j = 0; j < a.n_jobs && eligible; ++j) {
-      const Job& jb = a.jobs[j];
-      eligible = jb.vec && jb.flat_off % 8 == 0 && jb.shard_off % 8 == 0 && jb.len % 8 == 0;
-    }
-    if (eligible) return launch_step_tma<T>(a, s);
-  }
   switch (kind) {
     case Kind::kStep: fn = by_ranks<T, PickStep>(a.n_ranks); break;
     case Kind::kReduceScatter: fn = by_ranks<T, PickReduce>(a.n_ranks); break;
@@ -894,7 +947,7 @@ int launch_typed(Kind kind, const LaunchArgs& a, cudaStream_t s) {
     grid = 1;  // an empty launch still prepares the decision
   if (grid <= 0) return static_cast<int>(cudaGetLastError());
   void* args[] = {const_cast<LaunchArgs*>(&a)};
-  return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args, 0, s));
+  return static_cast<int>(launch_ordered(fn, dim3(grid), dim3(kThreads), args, 0, s, a.early));
 }
 
 }  // namespace zero

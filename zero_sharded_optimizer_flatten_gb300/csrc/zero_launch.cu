@@ -6,7 +6,6 @@
 #include <utility>
 
 #include "zero_kernels.cuh"
-#include "zero_kernels_tma.cuh"
 
 namespace zero {
 
@@ -94,7 +93,6 @@ __device__ void amp_decide(zero_amp_state& x, double sumsq, const AmpParams& p, 
 __global__ void __launch_bounds__(kFinThreads) k_amp_finalize(const NormPartial* partials,
                                                               int64_t n, zero_amp_state* st,
                                                               AmpHead* head, const AmpParams p) {
-  grid_dependency_begin();
   constexpr int64_t kAll = static_cast<int64_t>(kFinCtas) * kFinThreads;
   const float4* src = reinterpret_cast<const float4*>(partials);
   SqSum s = sq_zero();
@@ -150,38 +148,14 @@ int launch_amp_finalize(const NormPartial* partials, int64_t n_tiles, zero_amp_s
                         AmpHead* head, const AmpParams& p, void* stream) {
   AmpParams params = p;
   void* args[] = {const_cast<NormPartial**>(&partials), &n_tiles, &state, &head, &params};
-  return static_cast<int>(launch_ordered(reinterpret_cast<const void*>(&k_amp_finalize),
-                                         dim3(kFinCtas), dim3(kFinThreads), args, 0,
-                                         static_cast<cudaStream_t>(stream)));
+  return static_cast<int>(cudaLaunchKernel(reinterpret_cast<const void*>(&k_amp_finalize),
+                                           dim3(kFinCtas), dim3(kFinThreads), args, 0,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 int launch_amp_init(zero_amp_state* state, const zero_amp_state& init, void* stream) {
   k_amp_init<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(state, init);
   return static_cast<int>(cudaGetLastError());
-}
-
-// A persistent grid for `fn`: as many CTAs as fit on the GPU at once (with
-// smem_bytes of dynamic shared memory each), but no more than n_tiles.
-int resident_grid(const void* fn, int smem_bytes, int64_t n_tiles) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, int> cache;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find({fn, dev});
-  if (it == cache.end()) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-        cudaSuccess)
-      return -1;
-    int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem_bytes) !=
-        cudaSuccess)
-      return -1;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return -1;
-    it = cache.emplace(std::make_pair(fn, dev), (per_sm > 0 ? per_sm : 1) * sms).first;
-  }
-  return static_cast<int>(n_tiles < it->second ? n_tiles : it->second);
 }
 
 // The device error word: set by a kernel whose bounded wait gave up.
@@ -217,6 +191,38 @@ int take_device_error(void* stream) {
   return v;
 }
 
+// Bounded waits on a shared-memory mbarrier (the self-test below).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Poll the barrier's phase `parity` for at most limit_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // The failure path of a bounded wait, on purpose: wait on a barrier that no
 // thread ever arrives at, give up after limit_ns, raise the error word.
 __global__ void k_selftest_wait(int* err, unsigned long long limit_ns) {
@@ -238,7 +244,7 @@ int launch_selftest_wait(int64_t limit_ns, void* stream) {
 
 int launch_kernel(Kind kind, zero_dtype dtype, const LaunchArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((ZERO_DEBUG_BOUNDS || (ZERO_STEP_TMA != 0 && kind == Kind::kStep)) && !a.err) {
+  if (ZERO_DEBUG_BOUNDS && !a.err) {
     LaunchArgs& w = const_cast<LaunchArgs&>(a);
     w.err = device_error_word();
   }

@@ -25,7 +25,10 @@ void* g_dev_ptr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name only stands for the symbol, so the address is looked up
-// once per device, with that device current, and cached.
+// once per device, with that device current, and cached.  Under lazy module
+// loading the first lookup on a device also loads the module and commits the
+// array; the cached address stays valid for the life of the device's
+// context (a cudaDeviceReset would invalidate it).
 zero_status scratch_on_current_device(const char* fn, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
