@@ -496,6 +496,42 @@ class FlatRunner:
         return out, w.n_ranks * self.ext * 2, self.ext * 2
 
 
+class FloorRunner:
+    """zero_floor_probe with a FlatRunner's plan and buffers: the step's grid
+    and memory accesses without its arithmetic (kind 0: launch only; 1: the
+    loads; 2: the loads and stores), timed like the step."""
+
+    def __init__(self, run, kind):
+        self.Z, self.w, self.run, self.kind = run.Z, run.w, run, kind
+        self.bytes_per_step = run.bytes_per_step
+        self.elems = run.elems
+        self.kernel = "k_floor"
+        self.call = run.Z.FloorProbe(run.plan, kind, run.grads[0], run.master, run.m, run.v,
+                                     run.full16, rank_mask=run.mask,
+                                     bucket_elems=run.w.bucket_elems)
+
+    def step(self, t, events=None):
+        if events is not None:
+            events[0].record()
+        self.call()
+        if events is not None:
+            events[1].record()
+
+
+def floors(run, dev, steps, warmup, graph, flush_l2):
+    """Per-step time (us) of the step's launch shape alone, with its loads,
+    and with its loads and stores, next to the step itself, in one harness."""
+    out = {}
+    for kind, name in ((0, "launch_only_us"), (1, "loads_us"), (2, "loads_and_stores_us")):
+        r = time_steps(FloorRunner(run, kind), dev, steps, warmup, graph, flush_l2)
+        out[name] = 1e6 * r["kernel_s"]
+    out["step_us"] = 1e6 * time_steps(run, dev, steps, warmup, graph, flush_l2, t=10 ** 6)[
+        "kernel_s"]
+    out["note"] = ("zero_floor_probe: the step's grid, job table and memory accesses over the "
+                   "same buffers without its arithmetic, timed in the same harness")
+    return out
+
+
 class Zero3Runner:
     """The ZeRO-3 layer stream: per layer, all-gather the 8 ranks' 16-bit
     shards into the layer buffer, then the fused step writing each rank's
@@ -643,6 +679,12 @@ def time_steps(run, dev, steps, warmup, graph=True, flush_l2=False, dist=None, l
     wall0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    if flush is not None:
+        # the steps are enqueued one Python call at a time and timed by their
+        # own events: hold the GPU for a while first, so that the host is
+        # ahead of it and no step's events include time the GPU spends
+        # waiting for the host to enqueue it
+        torch.cuda._sleep(int(5e5 * steps))
     start.record(stream)
     if graph_obj is not None:
         graph_obj.replay()
@@ -723,6 +765,8 @@ def per_config(args, dev, clocks, peak):
         if w.zero3:
             out[key].update({"layers": run.layers, "layer_states": run.n_states,
                              "bytes_per_element": 46})
+        if opt.get("flush_l2"):
+            out[key]["floor"] = floors(run, dev, opt["steps"], opt["warmup"], True, True)
         del run
         gc.collect()
         torch.cuda.empty_cache()
@@ -855,6 +899,8 @@ def run_gpu(args, world, rank, local):
             line["config"]["prefetch_layer_buffers"] = run.prefetch
         line["config"]["layer_states"] = run.n_states
         line["config"]["layers"] = run.layers
+    if args.floor and not (w.zero3 or args.amp or args.offload):
+        line["floor"] = floors(run, dev, args.steps, args.warmup, args.graph, args.flush_l2)
     del run
     gc.collect()
     torch.cuda.empty_cache()
@@ -1167,6 +1213,9 @@ def main(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every timed step from Python instead of replaying the "
                          "steps captured in one CUDA graph (the default for flat groups)")
+    ap.add_argument("--floor", action="store_true",
+                    help="flat groups: also time the step's launch shape without arithmetic "
+                         "(launch only, loads, loads + stores) in the same harness")
     ap.add_argument("--unfused", action="store_true",
                     help="time the three unfused calls of a step separately")
     ap.add_argument("--gather-all", action="store_true",

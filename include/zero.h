@@ -436,6 +436,27 @@ zero_status zero_step_amp_noalloc(const zero_plan* plan, const void* const* grad
                                   void* d_state, uint64_t rank_mask, int64_t bucket_elems,
                                   void* stream);
 
+/*
+ * Measurement helper; the pages have no counterpart.  Launches, on `stream`,
+ * kernels with exactly the grid, job table and memory accesses zero_step
+ * would use for the same arguments (same plan, mask and buckets), but with
+ * none of its arithmetic, so that a benchmark can time the floor a launch of
+ * that shape reaches on this GPU:
+ *   kind 0  the launches alone (every CTA returns at once);
+ *   kind 1  every load of the step (the N gradient replicas, master, m, v),
+ *           no store;
+ *   kind 2  every load and every store of the step: master/m/v are written
+ *           back unchanged and full_flat16 (nullable) receives the master
+ *           rounded to 16 bits, which is what a step leaves there anyway.
+ * No buffer changes value.  Arguments, layouts, ownership and errors as for
+ * zero_step (no hyper-parameters, no shard outputs); kind outside 0..2 is
+ * ZERO_ERR_INVALID.  Asynchronous on `stream`.
+ */
+zero_status zero_floor_probe(const zero_plan* plan, int32_t kind, const void* const* grads,
+                             zero_dtype dtype, float* const* master, float* const* m,
+                             float* const* v, void* full_flat16, uint64_t rank_mask,
+                             int64_t bucket_elems, void* stream);
+
 /* Synchronize `stream` and report any asynchronous device error, and
  * ZERO_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check
  * (the device error word is then cleared). */

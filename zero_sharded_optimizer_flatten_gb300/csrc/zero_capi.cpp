@@ -495,6 +495,40 @@ extern "C" zero_status zero_step(const zero_plan* plan, const void* const* grads
   return run_buckets(fn, Kind::kStep, dtype, plan, rank_mask, bucket_elems, a, stream);
 }
 
+extern "C" zero_status zero_floor_probe(const zero_plan* plan, int32_t kind,
+                                        const void* const* grads, zero_dtype dtype,
+                                        float* const* master, float* const* m, float* const* v,
+                                        void* full_flat16, uint64_t rank_mask,
+                                        int64_t bucket_elems, void* stream) {
+  const char* fn = "zero_floor_probe";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (kind < 0 || kind > 2) return fail(ZERO_ERR_INVALID, "%s: kind must be 0, 1 or 2", fn);
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  if (full_flat16 && !aligned16(full_flat16))
+    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  ZERO_TRY(pending_error(fn));
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (!in_mask(rank_mask, r)) continue;
+    a.master[r] = master[r];
+    a.m[r] = m[r];
+    a.v[r] = v[r];
+  }
+  a.full16 = full_flat16;
+  a.n_ranks = plan->n_ranks;
+  const Kind k = kind == 0 ? Kind::kFloorLaunch : kind == 1 ? Kind::kFloorLoads : Kind::kFloorCopy;
+  return run_buckets(fn, k, dtype, plan, rank_mask, bucket_elems, a, stream);
+}
+
 extern "C" zero_status zero_amp_init(void* d_state, const zero_amp_config* cfg, void* stream) {
   const char* fn = "zero_amp_init";
   NvtxRange nvtx_range(fn);

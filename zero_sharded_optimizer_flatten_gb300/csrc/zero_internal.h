@@ -119,7 +119,10 @@ struct LaunchArgs {
   Job jobs[kMaxJobs];
 };
 
-enum class Kind { kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kShardStats, kAdamwAmp };
+enum class Kind {
+  kStep, kReduceScatter, kAdamw, kAllgather, kInit, kStats, kShardStats, kAdamwAmp,
+  kFloorLaunch, kFloorLoads, kFloorCopy  // measurement floors of kStep (zero_floor_probe)
+};
 
 // The decision of a mixed-precision step as the update kernel needs it.  The
 // decision kernel writes kAmpCopies copies, 64 bytes apart, at the start of

@@ -87,6 +87,7 @@ def lib():
                 "zero_allgather": [vp, vpp, ctypes.c_int, vp, u64, vp],
                 "zero_step": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vp, vpp, hp,
                               i64, u64, i64, vp],
+                "zero_floor_probe": [vp, i32, vpp, ctypes.c_int, vpp, vpp, vpp, vp, u64, i64, vp],
                 "zero_sync": [vp],
                 "zero_selftest_wait_timeout": [i64, vp],
                 "zero_reduce_scatter_range": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, u64, i64,
@@ -388,6 +389,26 @@ def zero_step(plan: Plan, grads, op, master, m, v, full_flat16, out16_shard, hpa
                            _stream(stream)))
 
 
+def zero_floor_probe(plan: Plan, kind: int, grads, master, m, v, full_flat16, rank_mask=None,
+                     bucket_elems=0, stream=None, dtype=None):
+    """Launches with zero_step's grid and memory accesses but none of its
+    arithmetic (kind 0: launch only; 1: loads; 2: loads and stores), for
+    timing the floor of a launch of that shape (see zero.h)."""
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    ms = _per_rank(plan, master, "master", mask, torch.float32)
+    mm = _per_rank(plan, m, "m", mask, torch.float32)
+    vv = _per_rank(plan, v, "v", mask, torch.float32)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    _check(lib().zero_floor_probe(plan.handle, int(kind), _ptrs(g), dt, _ptrs(ms), _ptrs(mm),
+                                  _ptrs(vv), full, mask, int(bucket_elems), _stream(stream)))
+
+
 def zero_sync(stream=None):
     _check(lib().zero_sync(_stream(stream)))
 
@@ -422,6 +443,32 @@ class ZeroStep:
         _check(lib().zero_step(self.plan.handle, self._g, self.dt, self.op, self._ms, self._mm,
                                self._vv, self._full, self._o16, ctypes.byref(self._hp),
                                int(step), self.mask, self.bucket, _stream(stream)))
+
+
+class FloorProbe:
+    """zero_floor_probe with its pointer arrays marshalled once (as ZeroStep),
+    so that timing loops measure the launches, not the marshalling."""
+
+    def __init__(self, plan: Plan, kind: int, grads, master, m, v, full_flat16, rank_mask=None,
+                 bucket_elems=0, dtype=None):
+        torch = _torch()
+        mask = _mask(plan, rank_mask)
+        self.plan, self.kind, self.mask, self.bucket = plan, int(kind), mask, int(bucket_elems)
+        self.dt = _sixteen(grads) if dtype is None else dtype
+        ext = plan.flat_extent(mask)
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        self._g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
+        self._ms = _ptrs(_per_rank(plan, master, "master", mask, torch.float32))
+        self._mm = _ptrs(_per_rank(plan, m, "m", mask, torch.float32))
+        self._vv = _ptrs(_per_rank(plan, v, "v", mask, torch.float32))
+        self._full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+        self._keep = (grads, master, m, v, full_flat16)
+
+    def __call__(self, stream=None):
+        _check(lib().zero_floor_probe(self.plan.handle, self.kind, self._g, self.dt, self._ms,
+                                      self._mm, self._vv, self._full, self.mask, self.bucket,
+                                      _stream(stream)))
 
 
 # ----------------------------------------------------------------------------
