@@ -291,11 +291,11 @@ def host_cpu() -> dict:
     return {"nproc": os.cpu_count(), "model": model}
 
 
-def cpu_baseline(w, budget_s: float = 10.0):
+def cpu_baseline(w, budget_s: float = 10.0, whole_bucket: bool = True):
     """The oracle on a bounded sample of the workload: one whole bucket for a
     bucketed group (the unit one launch of the step processes), else about
     `budget_s` seconds of single-threaded work."""
-    if w.bucket_elems:
+    if w.bucket_elems and whole_bucket:
         n = int(min(w.phi, w.bucket_elems))
         what = f"one whole {n}-element bucket (the first) of the {w.key} group"
     else:
@@ -741,6 +741,7 @@ def per_config(args, dev, clocks, peak):
 
     from zero_sharded_optimizer_flatten_gb300 import workloads as W
     out = {}
+    seen = set()
     for key, wkey, regime, opt in PER_CONFIG:
         if wkey == args.workload and not opt.get("flush_l2"):
             continue
@@ -770,6 +771,11 @@ def per_config(args, dev, clocks, peak):
         del run
         gc.collect()
         torch.cuda.empty_cache()
+        if not args.no_cpu_baseline and wkey not in seen:
+            # the oracle on a bounded sample of this group (about a second)
+            out[key]["cpu_baseline"] = cpu_baseline(w, args.per_config_cpu_budget,
+                                                    whole_bucket=False)
+            seen.add(wkey)
     return out
 
 
@@ -1189,6 +1195,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-config-cpu-budget", type=float, default=1.0,
+                    help="seconds of oracle work for each per_config record's cpu_baseline")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="skip the other groups' records (per_config) after the headline")
     ap.add_argument("--workload", default=WORKLOAD,

@@ -96,15 +96,18 @@ __global__ void __launch_bounds__(kFinThreads) k_amp_finalize(const NormPartial*
   constexpr int64_t kAll = static_cast<int64_t>(kFinCtas) * kFinThreads;
   const float4* src = reinterpret_cast<const float4*>(partials);
   SqSum s = sq_zero();
-  int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x;
-  for (; i + (kFinUnroll - 1) * kAll < n; i += kFinUnroll * kAll) {
+  // kFinUnroll of the thread's partials in flight at once (the last group
+  // predicated), added in increasing index order
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x; i < n;
+       i += kFinUnroll * kAll) {
     float4 q[kFinUnroll];
 #pragma unroll
-    for (int k = 0; k < kFinUnroll; ++k) q[k] = __ldcg(src + i + k * kAll);
+    for (int k = 0; k < kFinUnroll; ++k)
+      q[k] = i + k * kAll < n ? __ldcg(src + i + k * kAll) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kFinUnroll; ++k) s.add(q[k]);
+    for (int k = 0; k < kFinUnroll; ++k)
+      if (i + k * kAll < n) s.add(q[k]);
   }
-  for (; i < n; i += kAll) s.add(__ldcg(src + i));
   __shared__ SqSum warp_part[kFinThreads / 32];
   __shared__ int last;
   s = warp_sum(s);
