@@ -264,6 +264,18 @@ def oracle_rate(w, n_elems: int):
     return n_elems / el, el
 
 
+def host_available_bytes():
+    """MemAvailable of this host in bytes (None if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
 def host_cpu() -> dict:
     """The host the oracle runs on: its logical CPU count and model name."""
     model = None
@@ -809,7 +821,17 @@ def run_gpu(args, world, rank, local):
     bytes_per_launch, t = r["bytes_per_launch"], r["t"]
 
     e2e = None
-    if not w.zero3 and not args.amp and not args.offload and args.e2e_steps > 0:
+    pinned_need = (w.n_ranks + 1) * run.ext * 2 if hasattr(run, "ext") else 0
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    host_free = host_available_bytes()
+    if (not w.zero3 and not args.amp and not args.offload and args.e2e_steps > 0
+            and host_free is not None and pinned_need * local_world > 0.6 * host_free):
+        # every rank on this node would pin its own copy of the replicas
+        e2e = {"value": None, "unit": UNIT,
+               "skipped": f"the e2e leg pins {pinned_need / 1e9:.1f} GB of host memory per rank "
+                          f"({local_world} ranks on this node); only {host_free / 1e9:.0f} GB "
+                          f"are available"}
+    elif not w.zero3 and not args.amp and not args.offload and args.e2e_steps > 0:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         per_step, h2d, d2h = run.e2e(t, e2e_steps)
         link_s = per_step.pop("h2d_only")
