@@ -735,6 +735,46 @@ def time_steps(run, dev, steps, warmup, graph=True, flush_l2=False, dist=None, l
             "launches": launches, "t": t, "use_graph": use_graph, "window": (wall0, wall1)}
 
 
+def flushed_marginal(run, dev, steps, t=0, reps=3):
+    """Per-step time after an L2 flush, without per-step events: a CUDA graph
+    of `steps` (flush, step) pairs and one of `steps` flushes alone are each
+    replayed between two events; the difference over `steps` is what a step
+    adds after a flush (the median of `reps` pairs of replays).  The flush
+    reads a 256 MB buffer, twice the L2, so every step starts from DRAM."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def capture(with_step):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(steps):
+                torch.sum(flush, dim=0, out=sink)
+                if with_step:
+                    run.step(t + 1 + k)
+        torch.cuda.synchronize(dev)
+        return g
+    both, alone = capture(True), capture(False)
+    both.replay()
+    alone.replay()
+    torch.cuda.synchronize(dev)
+    per = []
+    for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        both.replay()
+        ev[1].record(stream)
+        alone.replay()
+        ev[2].record(stream)
+        torch.cuda.synchronize(dev)
+        per.append((ev[0].elapsed_time(ev[1]) - ev[1].elapsed_time(ev[2])) / 1e3 / steps)
+    del both, alone, flush
+    return statistics.median(per)
+
+
 def regime_text(run, use_graph, flush_l2):
     if flush_l2:
         return (f"flushed: a 256 MB buffer is read before every timed step, outside the "
@@ -780,6 +820,15 @@ def per_config(args, dev, clocks, peak):
                              "bytes_per_element": 46})
         if opt.get("flush_l2"):
             out[key]["floor"] = floors(run, dev, opt["steps"], opt["warmup"], True, True)
+            # the same regime without per-step events (see flushed_marginal)
+            mg = {"step_us": 1e6 * flushed_marginal(run, dev, opt["steps"], t=2 * 10 ** 6)}
+            for kind, name in ((0, "launch_only_us"), (2, "loads_and_stores_us")):
+                mg[name] = 1e6 * flushed_marginal(FloorRunner(run, kind), dev, opt["steps"])
+            mg["frac"] = run.bytes_per_step / (mg["step_us"] * 1e-6) / 1e9 / peak
+            mg["note"] = ("a CUDA graph of K (L2 flush, step) pairs replayed between two events, "
+                          "minus a graph of K flushes alone, over K: what a step adds after a "
+                          "flush, without per-step event records")
+            out[key]["graph_marginal"] = mg
         del run
         gc.collect()
         torch.cuda.empty_cache()
