@@ -340,6 +340,45 @@ def test_llama7b_rank0_shard_full_size_sampled():
     assert _sampled(W.WORKLOADS["llama7b_rank0"], 3, n_random=8000) > 8000
 
 
+def test_llama7b_rank0_shard_whole_buckets():
+    """Whole 50M-element buckets of rank 0's shard (the first, the last and two
+    seeded ones) over the three steps, every element against the oracle: the
+    step is element-wise, so whole buckets check everything a bucket launch
+    writes, including its tile and launch edges."""
+    w = W.WORKLOADS["llama7b_rank0"]
+    B = w.bucket_elems
+    seg = oracle.segments(list(w.numel), w.n_ranks, oracle.FLAT, w.align, 0)
+    assert (seg[:, 2] == seg[:, 3]).all()           # rank 0: shard index = flat index
+    S = int(seg[:, 4].sum())
+    nb = -(-S // B)
+    rng = np.random.default_rng(7)
+    picks = sorted({0, nb - 1, *[int(x) for x in rng.choice(np.arange(1, nb - 1), 2, False)]})
+    c = Case(w, with_oracle=False)
+    ext = c.plan.flat_extent(w.mask)
+    assert ext == S
+    dt, op, hp = dt_code(w), op_code(w), hp_oracle(HP)
+    ranges = [(b * B, min(S, (b + 1) * B)) for b in picks]
+    state = []
+    for lo, hi in ranges:
+        om = oracle.to_f32(u16(c.p16[lo:hi]), dt)
+        state.append([om, np.zeros_like(om), np.zeros_like(om), np.zeros(hi - lo, np.uint16)])
+    for t in range(1, 4):
+        g = [W.grads16(w, t, q, "cuda", 0, ext) for q in range(w.n_ranks)]
+        Z.zero_step(c.plan, g, w.op, c.master, c.m, c.v, c.full16[:ext], None, HP, t,
+                    rank_mask=w.mask, bucket_elems=B)
+        for (lo, hi), (om, mm, vv, out) in zip(ranges, state):
+            gs = np.stack([u16(x[lo:hi]) for x in g])
+            oracle.update_elements(gs, om, mm, vv, dt, op, hp, t, out16=out)
+        del g
+    torch.cuda.synchronize()
+    for b, (lo, hi), (om, mm, vv, out) in zip(picks, ranges, state):
+        what = f"bucket {b} [{lo}, {hi})"
+        assert_fp32_close(f32(c.master[0][lo:hi]), om, what + " master")
+        assert_fp32_close(f32(c.m[0][lo:hi]), mm, what + " m")
+        assert_fp32_close(f32(c.v[0][lo:hi]), vv, what + " v")
+        assert_16_close(u16(c.full16[lo:hi]), out, what + " full16", dtype_code=dt)
+
+
 @pytest.mark.parametrize("key", ["llama13b_layer", "llama13b_full_layer"])
 def test_llama13b_zero3_layer_pass_sampled(key):
     """Two layers of the ZeRO-3 stream (the 3 MLP matrices, or the whole
