@@ -86,3 +86,33 @@ def test_step_bytes():
     assert bench.step_bytes(109482240, 8) == 4598254080
     assert bench.step_bytes(1053760, 4) == 35827840
     assert bench.step_bytes(212336640, 8, n16_out=2) == 44 * 212336640
+
+
+def test_headline_and_per_config_groups():
+    """The default line times the LLaMA-7B rank-0 shard (42 B per element over
+    842,301,952 elements, 50M-element buckets: 17 launches); per_config names
+    every other group once, the tiny group in both regimes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    w = W.WORKLOADS[bench.WORKLOAD]
+    assert bench.WORKLOAD == "llama7b_rank0" and w.mask == 1 and w.bucket_elems == 50_000_000
+    S = 842_301_952
+    assert bench.step_bytes(S, w.n_ranks) == 35_376_681_984
+    assert -(-S // w.bucket_elems) == 17
+    keys = [k for k, *_ in bench.PER_CONFIG]
+    assert len(set(keys)) == len(keys)
+    groups = {wk for _, wk, _, _ in bench.PER_CONFIG}
+    assert groups == {"tiny_mlp", "bert_base", "toy_rr", "llama13b_layer"}
+    assert all(wk in W.WORKLOADS for wk in groups)
+    assert {k for k in keys if k.startswith("tiny_mlp/")} == {"tiny_mlp/back_to_back",
+                                                              "tiny_mlp/l2_flushed"}
+    flushed = [opt for k, _, _, opt in bench.PER_CONFIG if k == "tiny_mlp/l2_flushed"][0]
+    assert flushed.get("flush_l2") and flushed["warmup"] >= 3
+
+
+def test_host_available_bytes():
+    sys.path.insert(0, ROOT)
+    import bench
+    free = bench.host_available_bytes()
+    assert free is None or free > 0
