@@ -378,7 +378,8 @@ class FlatRunner:
     (bucketed if the workload says so).  Gradient buffers hold only the flat
     range the masked ranks own."""
 
-    def __init__(self, w, dev, grad_sets, amp=None, offload=False, from_shards=False):
+    def __init__(self, w, dev, grad_sets, amp=None, offload=False, from_shards=False,
+                 reduced=False):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
@@ -419,8 +420,13 @@ class FlatRunner:
             self.gsh = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
             self.state = Z.amp_state_tensor(dev)
             Z.zero_amp_init(self.state, amp)
+            self.ws_bucket = w.bucket_elems
+            if reduced and not self.ws_bucket:
+                # the reductions that write the partials go bucket by bucket;
+                # a group without buckets is one bucket of the whole buffer
+                self.ws_bucket = plan.padded
             self.ws = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan, self.mask,
-                                                                      w.bucket_elems)),
+                                                                      self.ws_bucket)),
                                   dtype=torch.uint8, device=dev)
 
             def make(g):
@@ -446,6 +452,24 @@ class FlatRunner:
             # shard read 4 B, update pass 4 + 24 + 2 B per element
             self.bytes_per_step = 34 * self.elems
             self.kernel = "k_shard_stats + k_amp_finalize + k_adamw_amp"
+        if amp is not None and reduced:
+            # the bucket reductions of a training loop already wrote the fp32
+            # shards and their tiles' sums of squares (untimed, once)
+            B = self.ws_bucket
+            red = Z.ReduceScatterBucketAmp(plan, self.grads[0], w.op, self.gsh, self.hp,
+                                           self.state, self.ws, rank_mask=self.mask,
+                                           bucket_elems=B)
+            for b in range(-(-plan.padded // B)):
+                red(b)
+
+            def step_reduced(t):
+                Z.zero_step_amp_reduced(plan, self.gsh, self.master, self.m, self.v, self.full16,
+                                        None, self.hp, amp, self.state, self.ws,
+                                        rank_mask=self.mask, bucket_elems=B)
+            self.calls = [step_reduced]
+            # update pass only: 4 + 24 + 2 B per element
+            self.bytes_per_step = 30 * self.elems
+            self.kernel = "k_amp_finalize + k_adamw_amp"
 
     def step(self, t, events=None):
         if events is not None:
@@ -637,10 +661,10 @@ PER_CONFIG = (
 
 
 def make_runner(w, dev, grad_sets=2, amp=None, offload=False, from_shards=False,
-                layer_states=40, prefetch=0):
+                layer_states=40, prefetch=0, reduced=False):
     if w.zero3:
         return Zero3Runner(w, dev, layer_states, prefetch)
-    return FlatRunner(w, dev, grad_sets, amp, offload, from_shards)
+    return FlatRunner(w, dev, grad_sets, amp, offload, from_shards, reduced)
 
 
 def time_steps(run, dev, steps, warmup, graph=True, flush_l2=False, dist=None, local=0, t=0):
@@ -859,7 +883,7 @@ def run_gpu(args, world, rank, local):
         amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
                           max_norm=args.max_norm)
     run = make_runner(w, dev, args.grad_sets, amp, args.offload, args.from_shards,
-                      args.layer_states, args.prefetch)
+                      args.layer_states, args.prefetch, args.reduced)
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
@@ -1280,6 +1304,9 @@ def main(argv=None):
     ap.add_argument("--from-shards", action="store_true",
                     help="--amp: the step from already reduce-scattered fp32 gradient shards "
                          "(zero_step_amp_shards)")
+    ap.add_argument("--reduced", action="store_true",
+                    help="--amp: the step after bucket reductions that also wrote the sums of "
+                         "squares (zero_reduce_scatter_bucket_amp, then zero_step_amp_reduced)")
     ap.add_argument("--offload", action="store_true",
                     help="keep the fp32 optimizer state in pinned host memory (ZeRO-Offload "
                          "over the host link)")

@@ -398,6 +398,57 @@ zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dtype,
                                  uint64_t rank_mask, int64_t bucket_elems, void* stream);
 
 /*
+ * One gradient bucket of a mixed-precision training step: the reduce-scatter
+ * of zero_reduce_scatter_range over the flat range
+ * [bucket_index * bucket_elems, min((bucket_index + 1) * bucket_elems,
+ * padded)) (bucket_elems <= 0: one bucket, the whole buffer), which also
+ * writes that bucket's per-tile sums of squares into `workspace`, numbered
+ * exactly as zero_step_amp numbers its tiles for the same plan, rank_mask
+ * and bucket_elems -- the reduction the pages overlap with the backward pass
+ * ("DeepSpeed ZeRO-2 ..." §2.2, §4.2: reduce_bucket_size, overlap_comm),
+ * with the overflow check's and the clipping norm's first pass folded into
+ * it, so that zero_step_amp_reduced needs no pass over the gradient shards
+ * for them.  Buckets may be reduced in any order, on any stream ordered
+ * before the step.  The launch holding the step's first tile also prepares
+ * the decision (it reads d_state's step count: no step on this state may be
+ * in flight).
+ *  hp: host pointer, read during the call (beta1, beta2);
+ *  d_state: the device state of zero_amp_init (read);
+ *  workspace: as zero_step_amp's, of at least
+ *    zero_amp_workspace_bytes(plan, rank_mask, bucket_elems) bytes.
+ * Errors: bucket_index outside the buckets, an undersized workspace, and
+ * the argument errors of zero_reduce_scatter_range (ZERO_ERR_INVALID /
+ * ZERO_ERR_ALIGN), before any launch.  A bucket whose range holds no element
+ * of a masked rank launches nothing.
+ */
+zero_status zero_reduce_scatter_bucket_amp(const zero_plan* plan, const void* const* grads,
+                                           zero_dtype dtype, zero_reduce_op op,
+                                           float* const* grad_shards,
+                                           const zero_adamw_hparams* hp, const void* d_state,
+                                           void* workspace, int64_t workspace_bytes,
+                                           uint64_t rank_mask, int64_t bucket_elems,
+                                           int64_t bucket_index, void* stream);
+
+/*
+ * The mixed-precision step after every bucket of the plan was reduced by
+ * zero_reduce_scatter_bucket_amp into grad_shards and `workspace` with the
+ * same rank_mask and bucket_elems since the last step on this state: only
+ * the decision kernel and the update run (no pass over the gradient shards
+ * for the norm: 30 bytes per element instead of zero_step_amp_shards's 34).
+ * Arguments and results as zero_step_amp_shards; the results equal
+ * zero_step_amp on the replicas with the same bucket_elems, bit for bit.
+ * Calling it without those reductions decides on whatever the workspace
+ * holds (nothing checks this on the device).
+ */
+zero_status zero_step_amp_reduced(const zero_plan* plan, zero_dtype dtype,
+                                  float* const* grad_shards, float* const* master,
+                                  float* const* m, float* const* v, void* full_flat16,
+                                  void* const* out16_shard, const zero_adamw_hparams* hp,
+                                  const zero_amp_config* cfg, void* d_state, void* workspace,
+                                  int64_t workspace_bytes, uint64_t rank_mask,
+                                  int64_t bucket_elems, void* stream);
+
+/*
  * zero_step_amp without a workspace argument, for callers that cannot
  * allocate device memory: code whose device memory all comes from a fixed
  * budget or pool it does not control, or that runs where a cudaMalloc /

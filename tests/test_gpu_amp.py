@@ -357,3 +357,70 @@ def test_amp_toy_model_full_size():
         assert_fp32_close(f32(c.v[r][it]), c.o_v[r][shard[sel]], f"v[{r}]")
     Ft = torch.from_numpy(F).cuda()
     assert_16_close(u16(c.full16[Ft]), c.o_full[F], "full16")
+
+
+@pytest.mark.parametrize("numel,N,mode,A,dtype,bucket", [
+    ((20000, 37, 4096, 3, 129), 4, "flat", 16, "fp16", 7000),
+    ((20000, 37, 4096, 3, 129), 4, "flat", 16, "fp16", 0),
+    (tuple(5 + (k * 7919) % 3001 for k in range(700)), 3, "round_robin", 1, "bf16", 300000),
+    ((70001,), 8, "flat", 2, "bf16", 9000),
+])
+def test_bucket_reductions_then_reduced_step_equal_the_fused_step(numel, N, mode, A, dtype,
+                                                                  bucket):
+    """Every bucket reduced by zero_reduce_scatter_bucket_amp (last bucket
+    first, as a backward pass fills them), then zero_step_amp_reduced: equal,
+    bit for bit, to zero_step_amp on the replicas with the same bucket size,
+    and to the oracle, through skipped overflows and clipping."""
+    w = W.small(numel, N, mode=mode, align=A, dtype=dtype, op="avg", outlier_frac=0.01)
+    # fp16: the first steps overflow (1 % of the entries are 100x larger)
+    # until the scale has halved to 2^14; bf16 never overflows
+    cfg = Z.AmpConfig(init_scale=2.0 ** 17, min_scale=1.0, window=3, hysteresis=2,
+                      max_norm=0.05)
+    ref = AmpCase(w, cfg, bucket=bucket)
+    got = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    P = ref.plan.padded
+    B = bucket if bucket > 0 else P
+    nb = -(-P // B)
+    for t in range(1, 9):
+        g = ref.grads_scaled(t, ref.ost.scale)
+        ref.gpu_step(g)
+        ref.oracle_step_amp(g)
+        n0 = Z.zero_launch_count()
+        for b in reversed(range(nb)):
+            Z.zero_reduce_scatter_bucket_amp(got.plan, g, "avg", got.gsh, HP, got.state, got.ws,
+                                             b, bucket_elems=bucket)
+        assert Z.zero_launch_count() - n0 >= 1
+        Z.zero_step_amp_reduced(got.plan, got.gsh, got.master, got.m, got.v, got.full16, None,
+                                HP, cfg, got.state, got.ws, bucket_elems=bucket)
+        torch.cuda.synchronize()
+        assert torch.equal(ref.state, got.state), t
+        assert torch.equal(ref.full16.view(torch.int16), got.full16.view(torch.int16)), t
+        for r in range(N):
+            for a, b_ in ((ref.master, got.master), (ref.m, got.m), (ref.v, got.v),
+                          (ref.gsh, got.gsh)):
+                assert torch.equal(a[r].view(torch.int32), b_[r].view(torch.int32)), (t, r)
+        ref.compare_state(f"step {t}")
+        ref.compare(f"bucket reductions, step {t}")
+    assert ref.ost.step >= 1
+    assert ref.ost.skipped >= 1 or dtype == "bf16"
+
+
+def test_bucket_amp_rejects_bad_arguments():
+    w = W.small((20000, 37), 2, mode="flat", align=16, dtype="fp16", op="avg")
+    cfg = Z.AmpConfig()
+    c = AmpCase(w, cfg, bucket=5000, with_oracle=False)
+    g = c.grads_scaled(1, 1.0)
+    nb = -(-c.plan.padded // 5000)
+    n0 = Z.zero_launch_count()
+    for b in (-1, nb):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_reduce_scatter_bucket_amp(c.plan, g, "avg", c.gsh, HP, c.state, c.ws, b,
+                                             bucket_elems=5000)
+        assert e.value.status == Z.ZERO_ERR_INVALID and "bucket" in str(e.value)
+    small = torch.empty(Z.zero_amp_workspace_bytes(c.plan, bucket_elems=5000) - 16,
+                        dtype=torch.uint8, device="cuda")
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_reduce_scatter_bucket_amp(c.plan, g, "avg", c.gsh, HP, c.state, small, 0,
+                                         bucket_elems=5000)
+    assert e.value.status == Z.ZERO_ERR_INVALID and "workspace" in str(e.value)
+    assert Z.zero_launch_count() == n0

@@ -114,9 +114,9 @@ def test_engine_mixed_precision_step_and_training():
     """fp16 student with a dynamic loss scale starting at 2^24 (the first
     backward passes overflow fp16 and are skipped while the scale falls),
     clipping at 1.0.  Each iteration, the engine's step (overlapped bucket
-    reductions, then zero_step_amp_shards) must equal zero_step_amp run on
-    copies of the engine's own gradient replicas and state, bit for bit; and
-    the model must train."""
+    reductions that also sum squares, then zero_step_amp_reduced) must equal
+    zero_step_amp run with the same bucket size on copies of the engine's own
+    gradient replicas and state, bit for bit; and the model must train."""
     teacher = _mlp(123, torch.float32)
     student = _mlp(1, torch.float16)
     cfg = Z.AmpConfig(init_scale=2.0 ** 24, min_scale=1.0, window=20, hysteresis=1,
@@ -149,7 +149,7 @@ def test_engine_mixed_precision_step_and_training():
         gsh = [torch.empty_like(x) for x in eng.grad_shards]
         ws = torch.empty_like(eng._workspace)
         Z.zero_step_amp(plan, grads, "avg", gsh, copies["master"], copies["m"], copies["v"],
-                        flat, None, hp, cfg, state, ws)
+                        flat, None, hp, cfg, state, ws, bucket_elems=eng.bucket_elems)
         eng.step()
         torch.cuda.synchronize()
         assert torch.equal(state, eng.amp_state), t
@@ -193,7 +193,8 @@ def test_engine_mixed_precision_step_other_layouts(mode, overlap, bucket):
         gsh = [torch.empty_like(x) for x in eng.grad_shards]
         ws = torch.empty_like(eng._workspace)
         Z.zero_step_amp(eng.plan, grads, "avg", gsh, copies["master"], copies["m"],
-                        copies["v"], flat, None, hp, cfg, state, ws)
+                        copies["v"], flat, None, hp, cfg, state, ws,
+                        bucket_elems=eng.bucket_elems)
         eng.step()
         torch.cuda.synchronize()
         assert torch.equal(state, eng.amp_state), t

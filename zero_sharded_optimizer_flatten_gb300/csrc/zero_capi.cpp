@@ -564,17 +564,22 @@ extern "C" zero_status zero_amp_workspace_bytes(const zero_plan* plan, uint64_t 
 namespace zero {
 namespace {
 
-// The mixed-precision step: with `grads`, reduce-scatter them into the fp32
-// shards while summing squares (k_stats); without, the shards already hold
-// the reduced gradient (k_shard_stats).  Then the decision kernel and the
-// update (k_adamw_amp).
+// Where the mixed-precision step's per-tile sums of squares come from.
+enum class AmpStats {
+  kReplicas,  // reduce-scatter the replicas into the fp32 shards while summing (k_stats)
+  kShards,    // the shards already hold the reduced gradient (k_shard_stats)
+  kDone,      // the bucket reductions already wrote every partial (no pass)
+};
+
+// The mixed-precision step: the sums of squares as `stats` says, then the
+// decision kernel and the update (k_adamw_amp).
 zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* grads,
-                     zero_dtype dtype, zero_reduce_op op, float* const* grad_shards,
-                     float* const* master, float* const* m, float* const* v, void* full_flat16,
-                     void* const* out16_shard, const zero_adamw_hparams* hp,
-                     const zero_amp_config* cfg, void* d_state, void* workspace,
-                     int64_t workspace_bytes, uint64_t rank_mask, int64_t bucket_elems,
-                     void* stream) {
+                     AmpStats stats_from, zero_dtype dtype, zero_reduce_op op,
+                     float* const* grad_shards, float* const* master, float* const* m,
+                     float* const* v, void* full_flat16, void* const* out16_shard,
+                     const zero_adamw_hparams* hp, const zero_amp_config* cfg, void* d_state,
+                     void* workspace, int64_t workspace_bytes, uint64_t rank_mask,
+                     int64_t bucket_elems, void* stream) {
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
   if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
@@ -621,9 +626,12 @@ zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* g
   a.beta1 = hp->beta1;
   a.beta2 = hp->beta2;
   set_scale(a, plan->n_ranks, op);
-  const Kind stats = grads ? Kind::kStats : Kind::kShardStats;
+  const Kind stats = stats_from == AmpStats::kReplicas ? Kind::kStats : Kind::kShardStats;
   int64_t done = 0;
-  ZERO_TRY(run_buckets(fn, stats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
+  if (stats_from == AmpStats::kDone)
+    done = tiles;  // numbered as the bucket reductions numbered them
+  else
+    ZERO_TRY(run_buckets(fn, stats, dtype, plan, rank_mask, bucket_elems, a, stream, &done));
   if (done == 0) {
     // no owned element: one empty reduction launch still prepares the
     // decision kernel (beta powers, counter)
@@ -664,8 +672,9 @@ extern "C" zero_status zero_step_amp(const zero_plan* plan, const void* const* g
   NvtxRange nvtx_range(fn);
   clear_error();
   if (!grads) return fail(ZERO_ERR_INVALID, "%s: grads is NULL", fn);
-  return amp_step(fn, plan, grads, dtype, op, grad_shards, master, m, v, full_flat16, out16_shard,
-                  hp, cfg, d_state, workspace, workspace_bytes, rank_mask, bucket_elems, stream);
+  return amp_step(fn, plan, grads, AmpStats::kReplicas, dtype, op, grad_shards, master, m, v,
+                  full_flat16, out16_shard, hp, cfg, d_state, workspace, workspace_bytes,
+                  rank_mask, bucket_elems, stream);
 }
 
 extern "C" zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dtype,
@@ -680,9 +689,86 @@ extern "C" zero_status zero_step_amp_shards(const zero_plan* plan, zero_dtype dt
   const char* fn = "zero_step_amp_shards";
   NvtxRange nvtx_range(fn);
   clear_error();
-  return amp_step(fn, plan, nullptr, dtype, ZERO_REDUCE_SUM, grad_shards, master, m, v,
-                  full_flat16, out16_shard, hp, cfg, d_state, workspace, workspace_bytes,
-                  rank_mask, bucket_elems, stream);
+  return amp_step(fn, plan, nullptr, AmpStats::kShards, dtype, ZERO_REDUCE_SUM, grad_shards,
+                  master, m, v, full_flat16, out16_shard, hp, cfg, d_state, workspace,
+                  workspace_bytes, rank_mask, bucket_elems, stream);
+}
+
+extern "C" zero_status zero_step_amp_reduced(const zero_plan* plan, zero_dtype dtype,
+                                             float* const* grad_shards, float* const* master,
+                                             float* const* m, float* const* v,
+                                             void* full_flat16, void* const* out16_shard,
+                                             const zero_adamw_hparams* hp,
+                                             const zero_amp_config* cfg, void* d_state,
+                                             void* workspace, int64_t workspace_bytes,
+                                             uint64_t rank_mask, int64_t bucket_elems,
+                                             void* stream) {
+  const char* fn = "zero_step_amp_reduced";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  return amp_step(fn, plan, nullptr, AmpStats::kDone, dtype, ZERO_REDUCE_SUM, grad_shards,
+                  master, m, v, full_flat16, out16_shard, hp, cfg, d_state, workspace,
+                  workspace_bytes, rank_mask, bucket_elems, stream);
+}
+
+extern "C" zero_status zero_reduce_scatter_bucket_amp(
+    const zero_plan* plan, const void* const* grads, zero_dtype dtype, zero_reduce_op op,
+    float* const* grad_shards, const zero_adamw_hparams* hp, const void* d_state,
+    void* workspace, int64_t workspace_bytes, uint64_t rank_mask, int64_t bucket_elems,
+    int64_t bucket_index, void* stream) {
+  const char* fn = "zero_reduce_scatter_bucket_amp";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, 1));
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  if (!d_state) return fail(ZERO_ERR_INVALID, "%s: d_state is NULL", fn);
+  if (!aligned16(d_state)) return fail(ZERO_ERR_ALIGN, "%s: d_state is not 16-byte aligned", fn);
+  const int64_t total = plan->padded;
+  const int64_t B = bucket_elems > 0 ? bucket_elems : std::max<int64_t>(total, 1);
+  const int64_t n_buckets = (total + B - 1) / B;
+  if (bucket_index < 0 || bucket_index >= std::max<int64_t>(n_buckets, 1))
+    return fail(ZERO_ERR_INVALID, "%s: bucket %" PRId64 " outside [0, %" PRId64 ")", fn,
+                bucket_index, std::max<int64_t>(n_buckets, 1));
+  const int64_t need =
+      kAmpHeadBytes + count_tiles(plan, rank_mask, bucket_elems) * static_cast<int64_t>(sizeof(NormPartial));
+  if (!workspace) return fail(ZERO_ERR_INVALID, "%s: workspace is NULL", fn);
+  if (!aligned16(workspace)) return fail(ZERO_ERR_ALIGN, "%s: workspace is not 16-byte aligned", fn);
+  if (workspace_bytes < need)
+    return fail(ZERO_ERR_INVALID, "%s: workspace holds %" PRId64 " bytes, needs %" PRId64, fn,
+                workspace_bytes, need);
+  ZERO_TRY(pending_error(fn));
+  // the bucket's first tile index: the tiles of the buckets before it, as
+  // zero_step_amp numbers them for this mask and bucket size
+  std::vector<Job> jobs;
+  int64_t base = 0;
+  for (int64_t k = 0; k < bucket_index; ++k) {
+    build_jobs(plan, rank_mask, k * B, std::min(total, (k + 1) * B), jobs);
+    for (const Job& j : jobs) base += (j.len + kTile - 1) / kTile;
+  }
+  const int64_t lo = bucket_index * B, hi = std::min(total, lo + B);
+  build_jobs(plan, rank_mask, lo, hi, jobs);
+  if (jobs.empty()) return ZERO_OK;
+  ArgsHolder h(new_args());
+  if (!h.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  LaunchArgs& a = *h.p;
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    a.grads[r] = grads[r];
+    if (in_mask(rank_mask, r)) a.gshard[r] = grad_shards[r];
+  }
+  AmpHead* head = static_cast<AmpHead*>(workspace);
+  a.head = head;
+  a.partials = reinterpret_cast<NormPartial*>(static_cast<char*>(workspace) + kAmpHeadBytes);
+  a.amp_state = static_cast<const zero_amp_state*>(d_state);
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+  set_scale(a, plan->n_ranks, op);
+  set_bounds(a, plan);
+  a.early = 0;
+  return launch_jobs(fn, Kind::kStats, dtype, a, jobs, stream, &base);
 }
 
 namespace {

@@ -21,9 +21,12 @@ With ``amp`` (an ``AmpConfig``) the engine is the fp16 ZeRO-2 loop of the
 pages' ds_config (fp16 loss_scale 0 = dynamic, loss_scale_window,
 hysteresis, min_loss_scale, gradient_clipping): ``backward`` multiplies each
 rank's loss by the current loss scale, read on the device from the state
-buffer (no host synchronisation), and ``step()`` runs the mixed-precision
-step on the reduced shards (overflow skip, scale update, clipping, AdamW,
-cast, gather; ``zero_step_amp_shards``).
+buffer (no host synchronisation); each bucket's reduction also writes its
+tiles' sums of squares (``zero_reduce_scatter_bucket_amp``), and ``step()``
+runs the rest of the mixed-precision step on the reduced shards (overflow
+skip, scale update, clipping, AdamW, cast, gather;
+``zero_step_amp_reduced``), bit-identical to ``zero_step_amp`` on the
+replicas with the same bucket size.
 
 The arithmetic is the library's (no compute happens here); this module only
 does bookkeeping and launches.
@@ -77,6 +80,7 @@ class ZeroEngine:
         Z.zero_init_shards(plan, self.flat16, self.master, self.m, self.v)
         # buckets over the flat index space; the tail padding needs no filling
         B = bucket_elems if bucket_elems > 0 else P
+        self.bucket_elems = B
         self.buckets = [(lo, min(lo + B, P)) for lo in range(0, P, B)]
         self._need = [max(0, min(hi, phi) - min(lo, phi)) for lo, hi in self.buckets]
         self._tensor_buckets = []
@@ -91,14 +95,20 @@ class ZeroEngine:
         self.reduction_stream = torch.cuda.Stream(dev) if overlap_comm else None
         self._reduce = Z.ReduceScatterRange(plan, self.grads, op, self.grad_shards)
         # mixed-precision controls: device state, its loss scale as a tensor
-        # view (the state's first field), the step's workspace
+        # view (the state's first field), the step's workspace; each bucket's
+        # reduction also writes its tiles' sums of squares into the workspace,
+        # so the step reads the gradient shards once (for the update)
         self.amp = amp
         if amp is not None:
             self.amp_state = Z.amp_state_tensor(dev)
             Z.zero_amp_init(self.amp_state, amp)
             self._scale = self.amp_state[:8].view(torch.float64)[0]
-            self._workspace = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan)),
+            self._workspace = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan,
+                                                                               bucket_elems=B)),
                                           dtype=torch.uint8, device=dev)
+            self._reduce_amp = Z.ReduceScatterBucketAmp(plan, self.grads, op, self.grad_shards,
+                                                        self.hp, self.amp_state, self._workspace,
+                                                        bucket_elems=B)
         self.step_count = 0
         self.launched_during_backward = 0
         self._current: Optional[int] = None
@@ -133,12 +143,15 @@ class ZeroEngine:
 
     def _launch(self, b: int):
         lo, hi = self.buckets[b]
-        if self.reduction_stream is None:
-            self._reduce(lo, hi)
-        else:
+        stream = None
+        if self.reduction_stream is not None:
             # the replica copies were queued on the current stream
             self.reduction_stream.wait_stream(torch.cuda.current_stream())
-            self._reduce(lo, hi, stream=self.reduction_stream)
+            stream = self.reduction_stream
+        if self.amp is not None:
+            self._reduce_amp(b, stream=stream)
+        else:
+            self._reduce(lo, hi, stream=stream)
         self._launched[b] = True
 
     # ------------------------------------------------------------------
@@ -175,9 +188,9 @@ class ZeroEngine:
         if self.amp is not None:
             # the step count that AdamW uses lives in the device state (skipped
             # steps do not count)
-            Z.zero_step_amp_shards(self.plan, self.grad_shards, self.master, self.m, self.v,
-                                   self.flat16, None, self.hp, self.amp, self.amp_state,
-                                   self._workspace)
+            Z.zero_step_amp_reduced(self.plan, self.grad_shards, self.master, self.m, self.v,
+                                    self.flat16, None, self.hp, self.amp, self.amp_state,
+                                    self._workspace, bucket_elems=self.bucket_elems)
         else:
             Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
                                     self.shard16, self.hp, self.step_count)

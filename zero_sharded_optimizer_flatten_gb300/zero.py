@@ -100,6 +100,10 @@ def lib():
                                   vpp, hp, ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
                 "zero_step_amp_shards": [vp, ctypes.c_int, vpp, vpp, vpp, vpp, vp, vpp, hp,
                                          ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
+                "zero_step_amp_reduced": [vp, ctypes.c_int, vpp, vpp, vpp, vpp, vp, vpp, hp,
+                                          ctypes.POINTER(AmpConfigC), vp, vp, i64, u64, i64, vp],
+                "zero_reduce_scatter_bucket_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, hp,
+                                                   vp, vp, i64, u64, i64, i64, vp],
                 "zero_step_amp_noalloc": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp,
                                           vpp, vp, vpp, hp, ctypes.POINTER(AmpConfigC), vp, u64,
                                           i64, vp],
@@ -577,7 +581,7 @@ def zero_step_amp(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
 
 def zero_step_amp_shards(plan: Plan, grad_shards, master, m, v, full_flat16, out16_shard,
                          hparams: AdamW, cfg: AmpConfig, d_state, workspace, rank_mask=None,
-                         bucket_elems=0, stream=None, dtype=None):
+                         bucket_elems=0, stream=None, dtype=None, _entry="zero_step_amp_shards"):
     """The mixed-precision step from already reduce-scattered fp32 gradient
     shards (read only): loss-scale check, clipping, AdamW, cast, gather.
     ``dtype`` (the 16-bit format) defaults to that of ``full_flat16`` or of
@@ -604,10 +608,62 @@ def zero_step_amp_shards(plan: Plan, grad_shards, master, m, v, full_flat16, out
     ws = _addr(workspace, "workspace")
     hp = hparams.c()
     c = cfg.c()
-    _check(L.zero_step_amp_shards(plan.handle, dt, _ptrs(gs), _ptrs(ms), _ptrs(mm), _ptrs(vv),
-                                  full, o16, ctypes.byref(hp), ctypes.byref(c),
-                                  _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
-                                  int(bucket_elems), _stream(stream)))
+    _check(getattr(L, _entry)(plan.handle, dt, _ptrs(gs), _ptrs(ms), _ptrs(mm), _ptrs(vv),
+                              full, o16, ctypes.byref(hp), ctypes.byref(c),
+                              _addr(d_state, "d_state", AMP_STATE_BYTES), ws, ws_bytes, mask,
+                              int(bucket_elems), _stream(stream)))
+
+
+def zero_step_amp_reduced(plan: Plan, grad_shards, master, m, v, full_flat16, out16_shard,
+                          hparams: AdamW, cfg: AmpConfig, d_state, workspace, rank_mask=None,
+                          bucket_elems=0, stream=None, dtype=None):
+    """The mixed-precision step after every bucket was reduced by
+    zero_reduce_scatter_bucket_amp (same mask and bucket size): decision and
+    update only (see zero.h)."""
+    zero_step_amp_shards(plan, grad_shards, master, m, v, full_flat16, out16_shard, hparams, cfg,
+                         d_state, workspace, rank_mask, bucket_elems, stream, dtype,
+                         _entry="zero_step_amp_reduced")
+
+
+class ReduceScatterBucketAmp:
+    """zero_reduce_scatter_bucket_amp with its pointer arrays marshalled once:
+    call(bucket_index, stream) reduces one bucket into the fp32 shards and
+    writes its per-tile sums of squares into the workspace."""
+
+    def __init__(self, plan: Plan, grads, op, grad_shards, hparams: AdamW, d_state, workspace,
+                 rank_mask=None, bucket_elems=0, dtype=None):
+        torch = _torch()
+        mask = _mask(plan, rank_mask)
+        self.plan, self.mask, self.bucket = plan, mask, int(bucket_elems)
+        self.dt = _sixteen(grads) if dtype is None else dtype
+        ext = plan.flat_extent(mask)
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        self._g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
+        self._gs = _ptrs(_per_rank(plan, grad_shards, "grad_shards", mask, torch.float32))
+        self.op = _OPS[op] if isinstance(op, str) else int(op)
+        self._hp = hparams.c()
+        self._state = _addr(d_state, "d_state", AMP_STATE_BYTES)
+        need = zero_amp_workspace_bytes(plan, mask, bucket_elems)
+        self._ws_bytes = (workspace.numel() * workspace.element_size()
+                          if not isinstance(workspace, int) else need)
+        self._ws = _addr(workspace, "workspace")
+        self._keep = (grads, grad_shards, d_state, workspace)
+
+    def __call__(self, bucket_index: int, stream=None):
+        _check(lib().zero_reduce_scatter_bucket_amp(
+            self.plan.handle, self._g, self.dt, self.op, self._gs, ctypes.byref(self._hp),
+            self._state, self._ws, self._ws_bytes, self.mask, self.bucket, int(bucket_index),
+            _stream(stream)))
+
+
+def zero_reduce_scatter_bucket_amp(plan: Plan, grads, op, grad_shards, hparams: AdamW, d_state,
+                                   workspace, bucket_index: int, rank_mask=None, bucket_elems=0,
+                                   stream=None, dtype=None):
+    """One bucket of the reduce-scatter that also writes its tiles' sums of
+    squares for zero_step_amp_reduced (see zero.h)."""
+    ReduceScatterBucketAmp(plan, grads, op, grad_shards, hparams, d_state, workspace,
+                           rank_mask, bucket_elems, dtype)(bucket_index, stream)
 
 
 def zero_step_amp_noalloc(plan: Plan, grads, op, grad_shards, master, m, v, full_flat16,
