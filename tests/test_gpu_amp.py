@@ -226,7 +226,10 @@ def test_amp_random_groups(seed):
     """Seeded random groups (the fused-step fuzz's draws: sizes, N up to 64,
     modes, formats, masks, buckets) under random controls: initial scales
     up to 2^24 (fp16 gradients then overflow until the scale has fallen),
-    windows, tolerances and clip thresholds; five calls each."""
+    windows, tolerances and clip thresholds; five calls each.  Each draw
+    also runs the bucket-reduction path (zero_reduce_scatter_bucket_amp over
+    the buckets in a seeded order, then zero_step_amp_reduced), which must
+    equal the fused step bit for bit."""
     from tests.test_gpu_fuzz import draw_case
     w, bucket, _, _ = draw_case(100 + seed)
     rng = np.random.default_rng(9000 + seed)
@@ -235,13 +238,28 @@ def test_amp_random_groups(seed):
                       hysteresis=int(rng.choice([1, 2, 3])),
                       max_norm=float(rng.choice([0.0, 1e-3, 0.05, 10.0])))
     c = AmpCase(w, cfg, bucket=bucket)
+    red = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    B = bucket if bucket > 0 else max(1, c.plan.padded)
+    order = rng.permutation(max(1, -(-c.plan.padded // B)))
     for t in range(1, 6):
         g = c.grads_scaled(t, c.ost.scale)
         c.gpu_step(g)
         c.oracle_step_amp(g)
+        for b in order:
+            Z.zero_reduce_scatter_bucket_amp(red.plan, g, w.op, red.gsh, HP, red.state, red.ws,
+                                             int(b), rank_mask=w.mask, bucket_elems=bucket)
+        Z.zero_step_amp_reduced(red.plan, red.gsh, red.master, red.m, red.v, red.full16, None,
+                                HP, cfg, red.state, red.ws, rank_mask=w.mask,
+                                bucket_elems=bucket, dtype=Z.ZERO_FP16 if w.dtype == "fp16"
+                                else Z.ZERO_BF16)
         torch.cuda.synchronize()
         c.compare_state(f"seed {seed} call {t}")
         c.compare(f"seed {seed} call {t}")
+        assert torch.equal(c.state, red.state), (seed, t)
+        assert torch.equal(c.full16.view(torch.int16), red.full16.view(torch.int16)), (seed, t)
+        for r in range(w.n_ranks):
+            for x, y in ((c.master, red.master), (c.m, red.m), (c.v, red.v)):
+                assert torch.equal(x[r].view(torch.int32), y[r].view(torch.int32)), (seed, t, r)
 
 
 def test_amp_many_tensors_number_tiles_across_launches():
