@@ -118,6 +118,43 @@ def test_many_tensors_need_several_launches():
         assert np.array_equal(u16(s16[r]), o16[r])
 
 
+def test_unfused_calls_with_several_launches():
+    """The unfused calls on the 700-tensor round-robin group, where each call
+    needs several launches (every launch after a call's first starts early):
+    zero_reduce_scatter bit for bit against the oracle's reduce-scatter,
+    zero_adamw_shard_step with 16-bit shard outputs and zero_allgather against
+    the oracle's step, over two steps."""
+    numel = _many_tensors()
+    w = W.small(numel, 3, mode="round_robin", align=1, dtype="fp16", op="sum")
+    c = Case(w)
+    gsh = [torch.empty(c.plan.shard_len(r), dtype=torch.float32, device="cuda") for r in range(3)]
+    s16 = [torch.empty(c.plan.shard_len(r), dtype=w.torch_dtype, device="cuda") for r in range(3)]
+    for t in (1, 2):
+        g = c.grads(t)
+        n0 = Z.zero_launch_count()
+        Z.zero_reduce_scatter(c.plan, g, "sum", gsh)
+        assert Z.zero_launch_count() - n0 >= 2
+        torch.cuda.synchronize()
+        orc = [np.zeros(c.plan.shard_len(r), np.float32) for r in range(3)]
+        oracle.reduce_scatter(list(numel), 3, oracle.ROUND_ROBIN, 1, dt_code(w), oracle.SUM,
+                              [u16(x) for x in g], orc)
+        for r in range(3):
+            assert np.array_equal(f32(gsh[r]).view(np.uint32), orc[r].view(np.uint32)), (t, r)
+        n0 = Z.zero_launch_count()
+        Z.zero_adamw_shard_step(c.plan, c.master, c.m, c.v, gsh, s16, HP, t)
+        Z.zero_allgather(c.plan, s16, c.full16)
+        assert Z.zero_launch_count() - n0 >= 4
+        c.oracle_step(g, t, hp_oracle(HP))
+        torch.cuda.synchronize()
+        c.compare(f"unfused, several launches, step {t}")
+        for r in range(3):
+            seg = c.o_seg[r]
+            o16 = np.zeros(c.plan.shard_len(r), np.uint16)
+            for k, toff, foff, soff, ln in seg:
+                o16[soff:soff + ln] = c.o_full[foff:foff + ln]
+            assert_16_close(u16(s16[r]), o16, f"shard16[{r}] step {t}", dtype_code=dt_code(w))
+
+
 @pytest.mark.parametrize("mode", ["flat", "round_robin"])
 def test_groups_without_elements(mode):
     """Every tensor empty: the plan has no element, a step launches nothing
