@@ -822,46 +822,77 @@ def per_config(args, dev, clocks, peak):
         if wkey == args.workload and not opt.get("flush_l2"):
             continue
         w = W.WORKLOADS[wkey]
-        run = make_runner(w, dev, prefetch=opt.get("prefetch", 0))
-        torch.cuda.synchronize(dev)
-        r = time_steps(run, dev, opt["steps"], opt["warmup"], graph=True,
-                       flush_l2=opt.get("flush_l2", False))
-        sec = r["elapsed"] / opt["steps"]
-        gbs = r["bytes_per_launch"] / r["kernel_s"] / 1e9
-        out[key] = {
-            "workload": w.title, "regime": regime, "steps": opt["steps"],
-            "warmup": opt["warmup"], "ms_per_step": 1e3 * sec,
-            "params_per_s": run.elems / sec, "elements_per_step": run.elems,
-            "bytes_per_step": run.bytes_per_step,
-            "gbs": gbs, "frac": gbs / peak,
-            "kernel": ("zero_zero3_pass (k_allgather + k_step per layer)"
-                       if getattr(run, "prefetch", 0) else run.kernel),
-            "gpu_launches": r["launches"],
-            "clocks": clocks.summary(*r["window"]),
-        }
-        if w.zero3:
-            out[key].update({"layers": run.layers, "layer_states": run.n_states,
-                             "bytes_per_element": 46})
-        if opt.get("flush_l2"):
-            out[key]["floor"] = floors(run, dev, opt["steps"], opt["warmup"], True, True)
-            # the same regime without per-step events (see flushed_marginal)
-            mg = {"step_us": 1e6 * flushed_marginal(run, dev, opt["steps"], t=2 * 10 ** 6)}
-            for kind, name in ((0, "launch_only_us"), (2, "loads_and_stores_us")):
-                mg[name] = 1e6 * flushed_marginal(FloorRunner(run, kind), dev, opt["steps"])
-            mg["frac"] = run.bytes_per_step / (mg["step_us"] * 1e-6) / 1e9 / peak
-            mg["note"] = ("a CUDA graph of K (L2 flush, step) pairs replayed between two events, "
-                          "minus a graph of K flushes alone, over K: what a step adds after a "
-                          "flush, without per-step event records")
-            out[key]["graph_marginal"] = mg
-        del run
+        try:
+            out[key] = one_config(args, dev, clocks, peak, w, regime, opt)
+        except Exception as e:  # one record's failure must not lose the line
+            out[key] = {"workload": w.title, "error": f"{type(e).__name__}: {e}"}
         gc.collect()
         torch.cuda.empty_cache()
-        if not args.no_cpu_baseline and wkey not in seen:
+        if not args.no_cpu_baseline and wkey not in seen and "error" not in out[key]:
             # the oracle on a bounded sample of this group (about a second)
             out[key]["cpu_baseline"] = cpu_baseline(w, args.per_config_cpu_budget,
                                                     whole_bucket=False)
             seen.add(wkey)
     return out
+
+
+def zero3_layer_states(w, dev, want: int) -> int:
+    """Distinct layer states of the ZeRO-3 pass that fit the device's free
+    memory (each holds fp32 master/m/v and a 16-bit shard: 14 B per element;
+    the gradient replicas and 3 layer buffers are shared): the largest
+    divisor of the layer count up to `want` that fits in 85 % of it."""
+    import torch
+    free, _ = torch.cuda.mem_get_info(dev)
+    per = 14 * w.phi
+    fixed = (2 * w.n_ranks + 2 * 3) * w.phi
+    fit = int((0.85 * free - fixed) // per)
+    for k in range(min(want, w.layers), 0, -1):
+        if w.layers % k == 0 and k <= fit:
+            return k
+    return 1
+
+
+def one_config(args, dev, clocks, peak, w, regime, opt):
+    """One per_config record: the group's runner, timed as the options say."""
+    import torch
+    want = 40
+    states = zero3_layer_states(w, dev, want) if w.zero3 else want
+    run = make_runner(w, dev, prefetch=opt.get("prefetch", 0), layer_states=states)
+    torch.cuda.synchronize(dev)
+    r = time_steps(run, dev, opt["steps"], opt["warmup"], graph=True,
+                   flush_l2=opt.get("flush_l2", False))
+    sec = r["elapsed"] / opt["steps"]
+    gbs = r["bytes_per_launch"] / r["kernel_s"] / 1e9
+    rec = {
+        "workload": w.title, "regime": regime, "steps": opt["steps"],
+        "warmup": opt["warmup"], "ms_per_step": 1e3 * sec,
+        "params_per_s": run.elems / sec, "elements_per_step": run.elems,
+        "bytes_per_step": run.bytes_per_step,
+        "gbs": gbs, "frac": gbs / peak,
+        "kernel": ("zero_zero3_pass (k_allgather + k_step per layer)"
+                   if getattr(run, "prefetch", 0) else run.kernel),
+        "gpu_launches": r["launches"],
+        "clocks": clocks.summary(*r["window"]),
+    }
+    if w.zero3:
+        rec.update({"layers": run.layers, "layer_states": run.n_states,
+                    "bytes_per_element": 46})
+        if run.n_states < want:
+            rec["note"] = (f"{run.n_states} distinct layer states cycled over the {run.layers} "
+                           f"layers: the device's free memory does not hold {want}")
+    if opt.get("flush_l2"):
+        rec["floor"] = floors(run, dev, opt["steps"], opt["warmup"], True, True)
+        # the same regime without per-step events (see flushed_marginal)
+        mg = {"step_us": 1e6 * flushed_marginal(run, dev, opt["steps"], t=2 * 10 ** 6)}
+        for kind, name in ((0, "launch_only_us"), (2, "loads_and_stores_us")):
+            mg[name] = 1e6 * flushed_marginal(FloorRunner(run, kind), dev, opt["steps"])
+        mg["frac"] = run.bytes_per_step / (mg["step_us"] * 1e-6) / 1e9 / peak
+        mg["note"] = ("a CUDA graph of K (L2 flush, step) pairs replayed between two events, "
+                      "minus a graph of K flushes alone, over K: what a step adds after a "
+                      "flush, without per-step event records")
+        rec["graph_marginal"] = mg
+    del run
+    return rec
 
 
 def run_gpu(args, world, rank, local):

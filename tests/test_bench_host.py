@@ -116,3 +116,19 @@ def test_host_available_bytes():
     import bench
     free = bench.host_available_bytes()
     assert free is None or free > 0
+
+
+def test_zero3_layer_states_fit_free_memory(monkeypatch):
+    """The 40-layer ZeRO-3 record keeps 40 distinct layer states when the
+    device has room (about 3 GB each for the 212M-element layer) and cycles
+    fewer, a divisor of 40, when it does not."""
+    sys.path.insert(0, ROOT)
+    import torch
+
+    import bench
+    from zero_sharded_optimizer_flatten_gb300 import workloads as W
+    w = W.WORKLOADS["llama13b_layer"]
+    for free_gb, want in ((275, 40), (100, 20), (40, 8), (5, 1)):
+        monkeypatch.setattr(torch.cuda, "mem_get_info",
+                            lambda dev=None, f=free_gb: (f * 10 ** 9, 280 * 10 ** 9))
+        assert bench.zero3_layer_states(w, None, 40) == want, free_gb
