@@ -255,6 +255,26 @@ def test_reduce_exact_on_small_integers(dtype, N):
     assert np.array_equal(a, (exact / N).astype(np.float32))
 
 
+def test_reduce_follows_rank_order():
+    """Replicas 1, 2^-24, 2^-24 (exact in binary16): in rank order 0, 1, 2 the
+    binary32 sum stays 1 (each 1 + 2^-24 is a tie that rounds to even); any
+    order that adds the two small terms first gives 1 + 2^-23.  The average is
+    that sum divided by 3 once (not the sum of thirds)."""
+    g = np.stack([_as16([1.0], oracle.FP16), _as16([2.0 ** -24], oracle.FP16),
+                  _as16([2.0 ** -24], oracle.FP16)])
+    s = oracle.reduce_elements(g, oracle.FP16, oracle.SUM)
+    assert s[0] == np.float32(1.0)
+    assert np.float32(1.0) + (np.float32(2.0 ** -24) + np.float32(2.0 ** -24)) != s[0]
+    a = oracle.reduce_elements(g, oracle.FP16, oracle.AVG)
+    assert a[0] == np.float32(1.0) / np.float32(3.0)
+    thirds = (np.float32(1.0) / np.float32(3.0) + np.float32(2.0 ** -24) / np.float32(3.0)) \
+        + np.float32(2.0 ** -24) / np.float32(3.0)
+    assert thirds != a[0]
+    # the reverse rank order reaches the other value
+    r = oracle.reduce_elements(g[::-1].copy(), oracle.FP16, oracle.SUM)
+    assert r[0] == np.float32(1.0 + 2.0 ** -23)
+
+
 @pytest.mark.parametrize("N", [2, 4, 8, 16])
 def test_reduce_error_bound(N):
     """Random fp16 gradients: |binary32 recursive sum - exact| <= gamma_{N-1} sum|g|."""
