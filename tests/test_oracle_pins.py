@@ -358,6 +358,27 @@ def test_adamw_constant_gradient_closed_form():
         assert np.max(np.abs(master - ref)) <= 8 * t * 2.0 ** -24 * (hp.lr + np.abs(ref).max())
 
 
+def test_adamw_first_step_decays_before_the_update():
+    """First step (m = v = 0, t = 1) at a large learning rate and decay:
+    p1 = p0 (1 - lr wd) - lr g / (|g| + eps).  Decaying after the update
+    instead would give (p0 - lr g / (|g| + eps)) (1 - lr wd), which differs
+    here by lr^2 wd = 5e-3 per unit gradient sign."""
+    hp = oracle.hparams(lr=0.1, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.5)
+    rng = np.random.default_rng(13)
+    n = 4096
+    p0 = rng.normal(0, 1.0, n).astype(np.float32)
+    g = rng.normal(0, 1e-2, n).astype(np.float32)
+    master, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adamw_elements(g, master, m, v, oracle.FP16, hp, 1)
+    pd, gd = p0.astype(np.float64), g.astype(np.float64)
+    u = hp.lr * gd / (np.abs(gd) + hp.eps)
+    first = pd * (1 - hp.lr * hp.weight_decay) - u
+    after = (pd - u) * (1 - hp.lr * hp.weight_decay)
+    err = np.abs(master - first)
+    assert err.max() <= 16 * 2.0 ** -24 * (np.abs(first).max() + hp.lr)
+    assert np.abs(after - first).min() >= 1e-3 > err.max()
+
+
 def test_adamw_zero_gradient_decays_only():
     hp = oracle.hparams()
     rng = np.random.default_rng(11)
