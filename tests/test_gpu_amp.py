@@ -442,3 +442,55 @@ def test_bucket_amp_rejects_bad_arguments():
                                          bucket_elems=5000)
     assert e.value.status == Z.ZERO_ERR_INVALID and "workspace" in str(e.value)
     assert Z.zero_launch_count() == n0
+
+
+@pytest.mark.parametrize("entry", ["fused", "shards", "reduced"])
+@pytest.mark.parametrize("with_full", [True, False])
+def test_amp_step_writes_16bit_shards(entry, with_full):
+    """The mixed-precision step with each rank's 16-bit shard as output (the
+    ZeRO-3 layout), with and without the gathered flat buffer, through each
+    of its three entry points: the shards, the buffer and the state equal the
+    oracle's (which writes the same shard outputs), over an fp16 overflow."""
+    w = W.small((20000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="fp16", op="avg",
+                outlier_frac=0.01)
+    cfg = Z.AmpConfig(init_scale=2.0 ** 16, min_scale=1.0, window=2, hysteresis=1,
+                      max_norm=0.05)
+    bucket = 8192
+    c = AmpCase(w, cfg, bucket=bucket)
+    s16 = [torch.full((c.plan.shard_len(r),), 7.0, dtype=w.torch_dtype, device="cuda")
+           for r in range(4)]
+    o16 = [oracle.f32_to_16(np.full(c.plan.shard_len(r), 7.0, np.float32).view(np.uint32),
+                            oracle.FP16) for r in range(4)]
+    full = c.full16 if with_full else None
+    o_full = c.o_full if with_full else None
+    P = c.plan.padded
+    for t in range(1, 6):
+        g = c.grads_scaled(t, c.ost.scale)
+        if entry == "fused":
+            Z.zero_step_amp(c.plan, g, "avg", c.gsh, c.master, c.m, c.v, full, s16, HP, cfg,
+                            c.state, c.ws, bucket_elems=bucket)
+        elif entry == "shards":
+            Z.zero_reduce_scatter(c.plan, g, "avg", c.gsh)
+            Z.zero_step_amp_shards(c.plan, c.gsh, c.master, c.m, c.v, full, s16, HP, cfg,
+                                   c.state, c.ws, bucket_elems=bucket)
+        else:
+            for b in range(-(-P // bucket)):
+                Z.zero_reduce_scatter_bucket_amp(c.plan, g, "avg", c.gsh, HP, c.state, c.ws, b,
+                                                 bucket_elems=bucket)
+            Z.zero_step_amp_reduced(c.plan, c.gsh, c.master, c.m, c.v, full, s16, HP, cfg,
+                                    c.state, c.ws, bucket_elems=bucket)
+        oracle.step_amp(list(w.numel), 4, mode_code(w), w.align, dt_code(w), op_code(w),
+                        [u16(x) for x in g], c.o_master, c.o_m, c.o_v, o_full, o16,
+                        hp_oracle(HP), _ocfg(cfg), c.ost, w.mask)
+        torch.cuda.synchronize()
+        c.compare_state(f"{entry} step {t}")
+        for r in range(4):
+            assert_fp32_close(f32(c.master[r]), c.o_master[r], f"{entry} master[{r}] step {t}")
+            assert_16_close(u16(s16[r]), o16[r], f"{entry} shard16[{r}] step {t}",
+                            dtype_code=dt_code(w))
+        if with_full:
+            assert_16_close(u16(c.full16), c.o_full, f"{entry} full16 step {t}",
+                            dtype_code=dt_code(w))
+        else:
+            assert not c.full16.any()               # never written
+    assert c.ost.skipped >= 1 and c.ost.step >= 1
