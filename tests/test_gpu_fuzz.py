@@ -17,8 +17,8 @@ import pytest
 import torch
 
 import oracle
-from tests._harness import (Case, assert_16_close, dt_code, hp_oracle, mode_code, op_code,
-                            u16)
+from tests._harness import (Case, assert_16_close, assert_fp32_close, dt_code, f32, hp_oracle,
+                            mode_code, op_code, u16)
 from zero_sharded_optimizer_flatten_gb300 import workloads as W
 from zero_sharded_optimizer_flatten_gb300 import zero as Z
 
@@ -110,3 +110,46 @@ def test_fuzz_covers_the_dispatch_paths():
     assert any(s for _, _, s, _ in draws)
     assert any(w.rank_mask is not None for w, *_ in draws)
     assert any(0 in w.numel for w, *_ in draws)
+
+
+@pytest.mark.parametrize("seed", range(0, N_CASES, 2))
+def test_random_group_unfused_calls_match_oracle(seed):
+    """The unfused calls on the same random draws (masks, buckets, N up to
+    64 so the generic kernels too): zero_reduce_scatter bit for bit against
+    the oracle's reduce-scatter; zero_adamw_shard_step (16-bit shard output
+    on or off) and zero_allgather of those shards against the oracle's step;
+    two steps."""
+    w, bucket, shard_out, hp = draw_case(seed)
+    what = (f"seed {seed}: numel {w.numel} N={w.n_ranks} {w.mode} A={w.align} {w.dtype} "
+            f"{w.op} mask={w.mask:#x} bucket={bucket} shards={shard_out}")
+    c = Case(w)
+    S = [c.plan.shard_len(r) if (w.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+    gsh = [torch.empty(n, dtype=torch.float32, device="cuda") for n in S]
+    s16 = [torch.empty(n, dtype=w.torch_dtype, device="cuda") for n in S]
+    for t in (1, 2):
+        g = c.grads(t)
+        Z.zero_reduce_scatter(c.plan, g, w.op, gsh, rank_mask=w.mask, bucket_elems=bucket)
+        torch.cuda.synchronize()
+        orc = [np.zeros(n, np.float32) for n in S]
+        oracle.reduce_scatter(list(w.numel), w.n_ranks, mode_code(w), w.align, dt_code(w),
+                              op_code(w), [u16(x) for x in g], orc, w.mask)
+        for r in range(w.n_ranks):
+            if S[r]:
+                assert np.array_equal(f32(gsh[r]).view(np.uint32), orc[r].view(np.uint32)), \
+                    f"{what} grad shard {r} step {t}"
+        Z.zero_adamw_shard_step(c.plan, c.master, c.m, c.v, gsh, s16 if shard_out else None, hp,
+                                t, rank_mask=w.mask,
+                                dtype=Z.ZERO_FP16 if w.dtype == "fp16" else Z.ZERO_BF16)
+        if shard_out:
+            Z.zero_allgather(c.plan, s16, c.full16, rank_mask=w.mask)
+        oracle.step(list(w.numel), w.n_ranks, mode_code(w), w.align, dt_code(w), op_code(w),
+                    [u16(x) for x in g], c.o_master, c.o_m, c.o_v, c.o_full, None,
+                    hp_oracle(hp), t, w.mask)
+    torch.cuda.synchronize()
+    for r in range(w.n_ranks):
+        if (w.mask >> r) & 1:
+            assert_fp32_close(f32(c.master[r]), c.o_master[r], f"{what} master[{r}]")
+            assert_fp32_close(f32(c.m[r]), c.o_m[r], f"{what} m[{r}]")
+            assert_fp32_close(f32(c.v[r]), c.o_v[r], f"{what} v[{r}]")
+    if shard_out:
+        assert_16_close(u16(c.full16), c.o_full, f"{what} full16", dtype_code=dt_code(w))
