@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import oracle
-from tests._harness import assert_16_close, assert_fp32_close, f32, hp_oracle, u16
+from tests._harness import (assert_16_close, assert_fp32_close, dt_code, f32, hp_oracle,
+                            mode_code, op_code, u16)
 from zero_sharded_optimizer_flatten_gb300 import workloads as W
 from zero_sharded_optimizer_flatten_gb300 import zero as Z
 
@@ -33,11 +34,16 @@ def _layers(w, plan, n_layers):
     out = []
     for layer in range(n_layers):
         p16 = W.params16(w, "cuda", plan.padded, layer=layer)
-        off = [plan.shards[r][0] for r in range(w.n_ranks)]
         S = [plan.shard_len(r) for r in range(w.n_ranks)]
+        shards = []
+        for r in range(w.n_ranks):       # rank r's 16-bit shard: its segments of p16
+            sh = torch.empty(S[r], dtype=w.torch_dtype, device="cuda")
+            for k, toff, foff, soff, ln in plan.segments(r):
+                sh[soff:soff + ln] = p16[foff:foff + ln]
+            shards.append(sh)
         L = {"grads": [W.grads16(w, 1, q, "cuda", 0, plan.padded, layer=layer)
                        for q in range(w.n_ranks)],
-             "shards16": [p16[off[r]:off[r] + S[r]].clone() for r in range(w.n_ranks)],
+             "shards16": shards,
              "master": [torch.empty(n, dtype=torch.float32, device="cuda") for n in S]}
         L["m"] = [torch.empty_like(x) for x in L["master"]]
         L["v"] = [torch.empty_like(x) for x in L["master"]]
@@ -53,21 +59,33 @@ def _oracle_layer(w, L):
     o = {"master": [], "m": [], "v": [], "shards16": [u16(x) for x in L["shards16"]],
          "grads": [u16(x) for x in L["grads"]]}
     for r in range(w.n_ranks):
-        seg = oracle.segments(list(w.numel), w.n_ranks, oracle.FLAT, w.align, r)
+        seg = oracle.segments(list(w.numel), w.n_ranks, mode_code(w), w.align, r)
         S = int(seg[:, 4].sum()) if len(seg) else 0
         mst = np.zeros(S, np.float32)
         for k, toff, foff, soff, ln in seg:
-            mst[soff:soff + ln] = oracle.to_f32(L["p16"][foff:foff + ln], oracle.BF16)
+            mst[soff:soff + ln] = oracle.to_f32(L["p16"][foff:foff + ln], dt_code(w))
         o["master"].append(mst)
         o["m"].append(np.zeros(S, np.float32))
         o["v"].append(np.zeros(S, np.float32))
     return o
 
 
+ZERO3_LAYOUTS = {
+    "flat_bf16_N4": dict(numel=(30000, 37, 4096, 3, 129), N=4, mode="flat", align=16,
+                         dtype="bf16", op="avg"),
+    "rr_fp16_N3_sum": dict(numel=(30000, 37, 4096, 3, 129, 777), N=3, mode="round_robin",
+                           align=1, dtype="fp16", op="sum"),
+}
+
+
+@pytest.mark.parametrize("layout", sorted(ZERO3_LAYOUTS))
 @pytest.mark.parametrize("n_bufs,two_streams", [(1, False), (1, True), (2, True), (3, True)])
-def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams):
-    w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
-    plan = Z.zero_plan_partitions(list(w.numel), 4, "flat", 16)
+def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams, layout):
+    cfg = ZERO3_LAYOUTS[layout]
+    N = cfg["N"]
+    w = W.small(cfg["numel"], N, mode=cfg["mode"], align=cfg["align"], dtype=cfg["dtype"],
+                op=cfg["op"])
+    plan = Z.zero_plan_partitions(list(w.numel), N, w.mode, w.align)
     n_layers = 5
     ref = _layers(w, plan, n_layers)
     got = _layers(w, plan, n_layers)
@@ -78,20 +96,21 @@ def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams):
     bufs = [torch.full((plan.padded,), 3.0, dtype=w.torch_dtype, device="cuda")
             for _ in range(n_bufs)]
     gather = torch.cuda.Stream() if two_streams else None
-    passer = Z.Zero3Pass(plan, got, bufs, "avg", HP)
+    passer = Z.Zero3Pass(plan, got, bufs, w.op, HP)
     hp = hp_oracle(HP)
+    md, dt, op = mode_code(w), dt_code(w), op_code(w)
     after_step1 = None
     for t in (1, 2):
         for layer in range(n_layers):
             L = ref[layer]
             Z.zero_allgather(plan, L["shards16"], ref_bufs[layer])
-            Z.zero_step(plan, L["grads"], "avg", L["master"], L["m"], L["v"], None,
+            Z.zero_step(plan, L["grads"], w.op, L["master"], L["m"], L["v"], None,
                         L["shards16"], HP, t)
             # the oracle's layer pass: gather, then the step writing the shards
             o = orc[layer]
-            oracle.allgather(list(w.numel), 4, oracle.FLAT, 16, o["shards16"], o_bufs[layer])
-            oracle.step(list(w.numel), 4, oracle.FLAT, 16, oracle.BF16, oracle.AVG, o["grads"],
-                        o["master"], o["m"], o["v"], None, o["shards16"], hp, t)
+            oracle.allgather(list(w.numel), N, md, w.align, o["shards16"], o_bufs[layer])
+            oracle.step(list(w.numel), N, md, w.align, dt, op, o["grads"], o["master"], o["m"],
+                        o["v"], None, o["shards16"], hp, t)
         passer(t, gather_stream=gather)
         if t == 1:
             torch.cuda.synchronize()
@@ -99,15 +118,15 @@ def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams):
     torch.cuda.synchronize()
     for layer in range(n_layers):
         o = orc[layer]
-        for r in range(4):
+        for r in range(N):
             for key in ("master", "m", "v", "shards16"):
                 assert torch.equal(got[layer][key][r], ref[layer][key][r]), (layer, key, r)
-            what = f"layer {layer} rank {r}"
+            what = f"{layout} layer {layer} rank {r}"
             assert_fp32_close(f32(got[layer]["master"][r]), o["master"][r], what + " master")
             assert_fp32_close(f32(got[layer]["m"][r]), o["m"][r], what + " m")
             assert_fp32_close(f32(got[layer]["v"][r]), o["v"][r], what + " v")
             assert_16_close(u16(got[layer]["shards16"][r]), o["shards16"][r], what + " shard16",
-                            dtype_code=oracle.BF16)
+                            dtype_code=dt)
     # each buffer holds the last gather that used it (of step 2): the oracle's
     # gather of the shards the pass wrote at step 1, bit for bit, and the
     # oracle's own layer buffer within the 16-bit bar
@@ -115,9 +134,9 @@ def test_zero3_pass_equals_oracle_and_serial_pieces(n_bufs, two_streams):
         last = max(l for l in range(n_layers) if l % n_bufs == b)
         assert torch.equal(bufs[b], ref_bufs[last])
         want = np.zeros(plan.padded, np.uint16)
-        oracle.allgather(list(w.numel), 4, oracle.FLAT, 16, after_step1[last], want)
+        oracle.allgather(list(w.numel), N, md, w.align, after_step1[last], want)
         assert np.array_equal(u16(bufs[b]), want), f"buffer {b}"
-        assert_16_close(u16(bufs[b]), o_bufs[last], f"buffer {b}", dtype_code=oracle.BF16)
+        assert_16_close(u16(bufs[b]), o_bufs[last], f"buffer {b}", dtype_code=dt)
 
 
 def test_zero3_pass_rejects_a_bad_layer_before_launching():
