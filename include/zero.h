@@ -46,6 +46,12 @@
  *  - Flat indices f run over the gathered flat buffer (length `padded` from
  *    zero_plan_total); shard indices i run over rank r's shard buffers
  *    (length from zero_plan_shard).
+ *  - A call may make several launches (one per bucket, and more when a
+ *    bucket holds more runs than one launch carries).  Launches of one call
+ *    that touch disjoint elements may run concurrently on the GPU; all of
+ *    them complete, with their writes visible, before work enqueued on the
+ *    stream after the call starts, so stream order between calls holds as
+ *    for single kernels (also inside captured CUDA graphs).
  */
 #ifndef ZERO_GB300_H_
 #define ZERO_GB300_H_
