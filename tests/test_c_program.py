@@ -6,7 +6,9 @@ and the CUDA runtime, and run as its own process (no Python or torch in it).
 bad arguments are rejected without a launch.  "gpu" mode: device buffers from
 cudaMalloc, zero_init_shards + two zero_step calls on 4 virtual ranks, the
 gathered bf16 buffer bit-identical to the oracle and the fp32 masters within
-1e-6 relative.
+1e-6 relative.  "amp" mode: the mixed-precision step from C, fused and as
+bucket reductions (last bucket first) plus zero_step_amp_reduced, the two
+bit-identical and both matching the oracle's mixed-precision step.
 """
 import glob
 import os
@@ -60,3 +62,11 @@ def test_c_program_steps_match_oracle(program):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     assert "gpu ok" in _run(program, "gpu")
+
+
+@pytest.mark.gpu
+def test_c_program_mixed_precision_paths_match_oracle(program):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    assert "amp ok" in _run(program, "amp")
