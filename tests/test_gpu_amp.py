@@ -494,3 +494,33 @@ def test_amp_step_writes_16bit_shards(entry, with_full):
         else:
             assert not c.full16.any()               # never written
     assert c.ost.skipped >= 1 and c.ost.step >= 1
+
+
+def test_reduced_path_full_size_equals_the_fused_step():
+    """The BERT-base group at full size (109,482,240 elements, 8 bf16
+    replicas), 5M-element buckets reduced last first, then
+    zero_step_amp_reduced: every buffer and the state equal zero_step_amp's
+    bit for bit over three clipped steps."""
+    w = W.WORKLOADS["bert_base"]
+    cfg = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=0, hysteresis=1, max_norm=0.5)
+    bucket = 5_000_000
+    a = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    b = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    nb = -(-a.plan.padded // bucket)
+    for t in range(1, 4):
+        g = a.grads_scaled(t, 1.0)
+        a.gpu_step(g)
+        step = Z.ReduceScatterBucketAmp(b.plan, g, "avg", b.gsh, HP, b.state, b.ws,
+                                        bucket_elems=bucket)
+        for k in reversed(range(nb)):
+            step(k)
+        Z.zero_step_amp_reduced(b.plan, b.gsh, b.master, b.m, b.v, b.full16, None, HP, cfg,
+                                b.state, b.ws, bucket_elems=bucket)
+        del g
+        torch.cuda.synchronize()
+        assert torch.equal(a.state, b.state), t
+    assert Z.read_amp_state(a.state).coef < 1.0          # clipping was active
+    assert torch.equal(a.full16.view(torch.int16), b.full16.view(torch.int16))
+    for r in range(w.n_ranks):
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.gsh, b.gsh)):
+            assert torch.equal(x[r].view(torch.int32), y[r].view(torch.int32)), r
