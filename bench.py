@@ -1050,9 +1050,11 @@ def run_gpu(args, world, rank, local):
 
 def run_offload_cpu(args, world, rank, local):
     """ZeRO-Offload with the CPU optimizer: per step the GPU reduce-scatters
-    the 8 replicas into pinned host fp32 shards, host threads run AdamW on the
-    host-resident state, the GPU all-gathers the host 16-bit shards into HBM.
-    Timed on the host clock (part of the step runs on the CPU)."""
+    the replicas into pinned host fp32 shards, host threads run AdamW + cast on
+    the host-resident state, the GPU all-gathers the host 16-bit shards into
+    HBM.  Timed two ways on the host clock (part of the step runs on the CPU):
+    the three calls one after another (with each phase's time), and
+    zero_offload_step, which overlaps them chunk by chunk."""
     import torch
 
     import zero_sharded_optimizer_flatten_gb300 as Z
@@ -1078,9 +1080,10 @@ def run_offload_cpu(args, world, rank, local):
     grads = [W.grads16(w, 1, q, dev, 0, plan.padded) for q in range(w.n_ranks)]
     hp = Z.AdamW()
     dt = Z.ZERO_BF16 if w.dtype == "bf16" else Z.ZERO_FP16
+    chunk = args.chunk if args.chunk >= 0 else max(1, -(-plan.padded // 8))
     phases = {"reduce": 0.0, "cpu_adamw": 0.0, "gather": 0.0}
 
-    def one(t, acc=None):
+    def serial(t, acc=None):
         t0 = time.perf_counter()
         Z.zero_reduce_scatter(plan, grads, w.op, gsh)
         Z.zero_sync()
@@ -1095,25 +1098,46 @@ def run_offload_cpu(args, world, rank, local):
             acc["reduce"] += t1 - t0
             acc["cpu_adamw"] += t2 - t1
             acc["gather"] += t3 - t2
+
+    def pipelined(t, acc=None):
+        Z.zero_offload_step(plan, grads, w.op, gsh, master, m, v, s16, full16, hp, t,
+                            chunk_elems=chunk, n_threads=args.threads)
+        Z.zero_sync()
+
     t = 0
-    for _ in range(args.warmup):
-        t += 1
-        one(t)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        t += 1
-        one(t, phases)
-    el = time.perf_counter() - t0
+
+    def timed(one, acc=None):
+        nonlocal t
+        for _ in range(args.warmup):
+            t += 1
+            one(t)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            t += 1
+            one(t, acc)
+        return time.perf_counter() - t0
+    el_serial = timed(serial, phases)
+    el = timed(pipelined)
+    ncpu = os.cpu_count() or 1
+    threads = {"pipelined": args.threads if args.threads > 0 else max(1, ncpu - 1),
+               "serial": args.threads if args.threads > 0 else ncpu}
     line = {"impl": "gb300", "metric": METRIC, "value": plan.phi * args.steps / el, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.title, "phi": plan.phi,
-                       "offload": "CPU optimizer: fp32 state in pinned host memory, AdamW on "
-                                  f"{args.threads if args.threads > 0 else os.cpu_count()} host "
-                                  "threads, GPU reduce-scatter and all-gather across the host link",
-                       "ms_per_phase": {k: 1e3 * x / args.steps for k, x in phases.items()},
-                       "timing": "host clock, device synchronised at each phase"}}
+                       "offload": "CPU optimizer: fp32 state in pinned host memory, AdamW + cast "
+                                  "on host threads, GPU reduce-scatter and all-gather across the "
+                                  f"host link, overlapped in chunks of {chunk} flat elements "
+                                  "(zero_offload_step)",
+                       "host_threads": threads,
+                       "serial": {"ms_per_step": 1e3 * el_serial / args.steps,
+                                  "ms_per_phase": {k: 1e3 * x / args.steps
+                                                   for k, x in phases.items()},
+                                  "calls": "zero_reduce_scatter, zero_sync, "
+                                           "zero_cpu_adamw_shard_step, zero_allgather, zero_sync"},
+                       "host_bytes_per_element": 30,
+                       "timing": "host clock around each step, device synchronised at its end"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -1362,6 +1386,9 @@ def main(argv=None):
                     help="ZeRO-Offload with the CPU optimizer (host threads run AdamW)")
     ap.add_argument("--threads", type=int, default=0,
                     help="--offload-cpu: host threads (0 = all hardware threads)")
+    ap.add_argument("--chunk", type=int, default=-1,
+                    help="--offload-cpu: flat elements per pipelined chunk (-1: an eighth of "
+                         "the buffer; 0: one chunk)")
     ap.add_argument("--engine", action="store_true",
                     help="time a training iteration through the autograd-driven engine")
     ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")

@@ -229,14 +229,57 @@ zero_status zero_adamw_shard_step(const zero_plan* plan, float* const* master, f
  * same binary32 operations in the same order, so the results equal the GPU
  * update bit for bit.  It runs only when called: the usual offload step is
  * zero_reduce_scatter into pinned host grad_shards, zero_sync, this call,
- * then zero_allgather from the pinned host 16-bit shards.  Synchronous;
- * n_threads <= 0 uses every hardware thread.
+ * then zero_allgather from the pinned host 16-bit shards (zero_offload_step
+ * runs that sequence overlapped).  Synchronous; the masked ranks' shards are
+ * split into n_threads equal slices (n_threads <= 0: every hardware thread;
+ * the calling thread takes the first slice).
  */
 zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* const* master,
                                       float* const* m, float* const* v,
                                       const float* const* grad_shards, void* const* out16_shard,
                                       zero_dtype dtype, const zero_adamw_hparams* hp,
                                       int64_t step, uint64_t rank_mask, int32_t n_threads);
+
+/*
+ * ZeRO-Offload with the CPU optimizer, pipelined ([ZeRO-2 blog] §4.5:
+ * offload_optimizer to the CPU, DeepSpeedCPUAdam, pinned-memory gradient
+ * buffers; the pipelining is this library's).  The result is that of
+ *   zero_reduce_scatter(grads -> grad_shards); zero_sync;
+ *   zero_cpu_adamw_shard_step(master, m, v, grad_shards -> out16_shard);
+ *   zero_allgather(out16_shard -> full_flat16)
+ * element for element and bit for bit, but the flat index space is cut into
+ * chunks of chunk_elems elements: the device reduces every chunk in turn,
+ * host threads update chunk k as soon as its reduction has completed (while
+ * the device still reduces the chunks after it), and chunk k's all-gather is
+ * enqueued as soon as the host has written its 16-bit values.
+ *  grads: the N flat replicas (device, or pinned host memory).
+ *  grad_shards, out16_shard: PINNED (or managed) host memory the device
+ *    writes (fp32 reduced gradient) and reads (16-bit shard) across the host
+ *    link; checked with cudaPointerGetAttributes (ZERO_ERR_INVALID otherwise).
+ *  master, m, v: host memory (pinned or not; never device memory), updated
+ *    by the host threads only.
+ *  full_flat16: device memory, or NULL for no gather (the 16-bit shards are
+ *    still written).
+ *  chunk_elems <= 0: one chunk (no overlap); at most 4096 chunks.
+ *  n_threads: host threads that update (at most 1024); <= 0: every hardware
+ *    thread but one, which is left to the calling thread (it sleeps on the
+ *    device's events and launches the gathers).
+ * Each thread updates an equal slice of every chunk, so the host part takes
+ * what streaming 30 bytes per element through host memory takes; the device
+ * traffic across the host link shares that memory.
+ * Blocking: returns when every host update is done and every gather is
+ * enqueued on `stream` (the gathers complete asynchronously; zero_sync or a
+ * later call on `stream` orders after them).  It waits for the device in the
+ * middle, so it cannot be captured in a CUDA graph (ZERO_ERR_UNSUPPORTED
+ * while `stream` is capturing).  A ZERO_ERR_CUDA during the call may leave
+ * some chunks updated and others not.
+ */
+zero_status zero_offload_step(const zero_plan* plan, const void* const* grads, zero_dtype dtype,
+                              zero_reduce_op op, float* const* grad_shards, float* const* master,
+                              float* const* m, float* const* v, void* const* out16_shard,
+                              void* full_flat16, const zero_adamw_hparams* hp, int64_t step,
+                              uint64_t rank_mask, int64_t chunk_elems, int32_t n_threads,
+                              void* stream);
 
 /*
  * All-gather ([ZeRO-2 blog] §4.4): full_flat16[f] = shards16[r][i] for every

@@ -48,3 +48,53 @@ def test_cpu_adamw_rejects_bad_arguments():
         Z.zero_cpu_adamw_shard_step(plan, x, x, x, x, None, Z.AdamW(), 0, Z.ZERO_BF16)
     with pytest.raises(Z.ZeroError):
         Z.zero_cpu_adamw_shard_step(plan, x, x, x, [x[0], 0], None, Z.AdamW(), 1, Z.ZERO_BF16)
+
+
+
+def _nan_mask(u, bits, dtype=None):
+    """NaN positions of binary32 (bits 32) or 16-bit patterns of `dtype`."""
+    if bits == 32:
+        return np.isnan(u.view(np.float32))
+    exp_mask, man_mask = (0x7F80, 0x007F) if dtype == Z.ZERO_BF16 else (0x7C00, 0x03FF)
+    return ((u & exp_mask) == exp_mask) & ((u & man_mask) != 0)
+
+
+def _same_or_both_nan(got, want, bits, dtype=None):
+    """Bit-equal, except that a NaN need only be a NaN on both sides (its
+    payload follows the host's NaN propagation, which IEEE leaves open)."""
+    ng, nw = _nan_mask(got, bits, dtype), _nan_mask(want, bits, dtype)
+    assert np.array_equal(ng, nw)
+    assert np.array_equal(got[~ng], want[~nw])
+
+
+@pytest.mark.parametrize("dtype", [Z.ZERO_BF16, Z.ZERO_FP16], ids=["bf16", "fp16"])
+def test_cpu_adamw_non_finite_values_and_no_cast(dtype):
+    """Infinite and NaN gradients, gradients whose square overflows binary32,
+    master values past the fp16 range and a bf16 rounding tie: the host loop
+    (vectorised, with the cast in the same pass) gives the oracle's IEEE
+    results; without a 16-bit output it updates the state identically."""
+    plan = Z.zero_plan_partitions([4099], 1, "flat", 1)
+    n = plan.shard_len(0)
+    rng = np.random.default_rng(7)
+    hp = Z.AdamW(lr=1e-3, weight_decay=0.01)
+    ohp = oracle.hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay)
+    mst = rng.normal(0, 0.02, n).astype(np.float32)
+    mst[:6] = [7e4, -7e4, 65519.0, 65520.0, 1.0 + 2.0 ** -8, 3e38]
+    g = rng.normal(0, 1e-2, n).astype(np.float32)
+    g[6:12] = [np.inf, -np.inf, np.nan, 3e38, -2e19, 0.0]
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    om, omm, ov = mst.copy(), m.copy(), v.copy()
+    nm, nmm, nv = mst.copy(), m.copy(), v.copy()
+    out = np.zeros(n, np.uint16)
+    o16 = np.zeros(n, np.uint16)
+    for t in (1, 2):
+        Z.zero_cpu_adamw_shard_step(plan, [mst], [m], [v], [g], [out], hp, t, dtype)
+        Z.zero_cpu_adamw_shard_step(plan, [nm], [nmm], [nv], [g], None, hp, t, dtype)
+        oracle.adamw_elements(g, om, omm, ov, dtype, ohp, t, out16=o16)
+        for got, want in ((mst, om), (m, omm), (v, ov), (nm, om), (nmm, omm), (nv, ov)):
+            _same_or_both_nan(got.view(np.uint32), want.view(np.uint32), 32)
+        _same_or_both_nan(out, o16, 16, dtype)
+    assert np.isnan(mst[6:9]).all()          # inf / inf and NaN reach the master
+    assert np.isinf(v[9:11]).all()           # the squares of 3e38 and 2e19 overflow
+    assert np.isfinite(mst[9:11]).all()      # ... so the step m / den is 0

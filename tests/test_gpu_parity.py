@@ -554,6 +554,108 @@ def test_cpu_optimizer_offload_pipeline():
     assert_16_close(u16(full), dev_case.o_full, "full16", dtype_code=dt_code(w))
 
 
+
+def _host_offload_state(c: Case):
+    """Host copies of a fresh case's shards: master in pinned memory, m/v in
+    pageable host memory (allowed), pinned fp32 gradient and 16-bit shards."""
+    S = [c.plan.shard_len(r) if (c.w.mask >> r) & 1 else 0 for r in range(c.w.n_ranks)]
+    pin = lambda n, dt: torch.zeros(n, dtype=dt, pin_memory=True)  # noqa: E731
+    hm = [c.master[r].cpu().pin_memory() for r in range(c.w.n_ranks)]
+    hmm = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hv = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hg = [pin(n, torch.float32) for n in S]
+    h16 = [pin(n, c.w.torch_dtype) for n in S]
+    return hm, hmm, hv, hg, h16
+
+
+@pytest.mark.parametrize("numel,N,mode,dtype,op,mask,chunk,threads", [
+    ((30000, 37, 4096, 3, 129), 4, "flat", "bf16", "avg", None, None, 0),
+    ((30000, 37, 4096, 3, 129), 4, "flat", "bf16", "avg", None, 0, 3),
+    ((30000, 37, 4096, 3, 129), 4, "flat", "bf16", "avg", None, 1000, 5),
+    ((30000, 37, 4096, 3, 129), 4, "flat", "fp16", "sum", 0b1010, 2999, 2),
+    ((5000, 7, 12000, 1, 333, 9000), 3, "round_robin", "fp16", "sum", None, 4097, 4),
+    ((20000, 17), 5, "flat", "bf16", "avg", None, 13, 1),
+])
+def test_pipelined_offload_step(numel, N, mode, dtype, op, mask, chunk, threads):
+    """zero_offload_step (device reduce of chunk k+1 while host threads update
+    chunk k, gather of each finished chunk) against the oracle, and bit for bit
+    against the serial offload calls, over chunk sizes that cut tensors,
+    shards and tiles anywhere, one chunk, rank masks and both layouts."""
+    w = W.small(numel, N, mode=mode, align=16, dtype=dtype, op=op, rank_mask=mask)
+    c = Case(w)
+    plan = c.plan
+    hm, hmm, hv, hg, h16 = _host_offload_state(c)
+    sm, smm, sv, sg, s16 = _host_offload_state(c)
+    full = torch.zeros_like(c.full16)
+    sfull = torch.zeros_like(c.full16)
+    dt = Z.ZERO_BF16 if dtype == "bf16" else Z.ZERO_FP16
+    for t in (1, 2, 3):
+        g = c.grads(t)
+        Z.zero_offload_step(plan, g, op, hg, hm, hmm, hv, h16, full, HP, t, rank_mask=w.mask,
+                            chunk_elems=chunk, n_threads=threads)
+        Z.zero_reduce_scatter(plan, g, op, sg, rank_mask=w.mask)
+        Z.zero_sync()
+        Z.zero_cpu_adamw_shard_step(plan, sm, smm, sv, sg, s16, HP, t, dt, rank_mask=w.mask)
+        Z.zero_allgather(plan, s16, sfull, rank_mask=w.mask)
+        c.oracle_step(g, t, hp_oracle(HP))
+    torch.cuda.synchronize()
+    for r in range(N):
+        if not (w.mask >> r) & 1:
+            continue
+        for got, ser, ref, what in ((hm, sm, c.o_master, "master"), (hmm, smm, c.o_m, "m"),
+                                    (hv, sv, c.o_v, "v")):
+            assert torch.equal(got[r], ser[r]), f"{what}[{r}] differs from the serial calls"
+            assert_fp32_close(got[r].numpy(), ref[r], f"offload {what}[{r}]")
+        assert torch.equal(h16[r], s16[r])
+        seg = c.o_seg[r]
+        want = np.concatenate([c.o_full[f:f + n] for _, _, f, _, n in seg]) if len(seg) else \
+            np.zeros(0, np.uint16)
+        assert_16_close(u16(h16[r]), want, f"offload shard16[{r}]", dtype_code=dt_code(w))
+    assert torch.equal(full, sfull)
+    owned = np.zeros(plan.padded, bool)
+    for r in range(N):
+        if (w.mask >> r) & 1:
+            for _, _, f, _, n in c.o_seg[r]:
+                owned[f:f + n] = True
+    assert_16_close(u16(full)[owned], c.o_full[owned], "offload full16", dtype_code=dt_code(w))
+    assert not u16(full)[~owned].any(), "an unmasked rank's elements were written"
+
+
+def test_pipelined_offload_step_rejects_bad_arguments_without_launching():
+    w = W.small((30000, 37), 2, mode="flat", align=16, dtype="bf16", op="avg")
+    c = Case(w, with_oracle=False)
+    hm, hmm, hv, hg, h16 = _host_offload_state(c)
+    g = c.grads(1)
+    before = Z.zero_launch_count()
+    # raw addresses pass the binding's own checks and reach the library's
+    pageable = [torch.zeros(c.plan.shard_len(r), dtype=torch.float32) for r in range(2)]
+    with pytest.raises(Z.ZeroError, match="pinned"):
+        Z.zero_offload_step(c.plan, g, "avg", [t.data_ptr() for t in pageable], hm, hmm, hv,
+                            h16, c.full16, HP, 1)
+    with pytest.raises(Z.ZeroError, match="device memory"):
+        Z.zero_offload_step(c.plan, g, "avg", hg, [t.data_ptr() for t in c.master], hmm, hv,
+                            h16, c.full16, HP, 1)
+    with pytest.raises(Z.ZeroError, match="chunks"):
+        Z.zero_offload_step(c.plan, g, "avg", hg, hm, hmm, hv, h16, c.full16, HP, 1,
+                            chunk_elems=7)
+    with pytest.raises(Z.ZeroError, match="must be >= 1"):
+        Z.zero_offload_step(c.plan, g, "avg", hg, hm, hmm, hv, h16, c.full16, HP, 0)
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    x = torch.zeros(4, device="cuda")
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        x.add_(1)
+        try:
+            with pytest.raises(Z.ZeroError, match="captured"):
+                Z.zero_offload_step(c.plan, g, "avg", hg, hm, hmm, hv, h16, c.full16, HP, 1,
+                                    stream=side)
+        finally:
+            graph.capture_end()
+    torch.cuda.synchronize()
+    assert Z.zero_launch_count() == before
+    assert not any(t.any() for t in h16) and not any(t.any() for t in hg)
+
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_non_finite_gradients_propagate_like_the_oracle(dtype):
     """+inf, -inf and NaN in one replica: the plain step propagates them as

@@ -13,6 +13,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <condition_variable>
+#include <mutex>
 #include <new>
 #include <thread>
 #include <vector>
@@ -235,6 +237,39 @@ LaunchArgs* new_args() {
   return a;
 }
 
+// One host update piece: elements [off, off + len) of rank r's shard.
+struct HostPiece {
+  int r;
+  int64_t off, len;
+};
+
+// The host optimizer's operands (host arrays, per rank).
+struct HostUpdate {
+  StepScalars sc;
+  zero_dtype dtype;
+  float* const* master;
+  float* const* m;
+  float* const* v;
+  const float* const* grad_shards;
+  void* const* out16;  // nullable; entries nullable
+
+  // Update elements [b0, b1) of the concatenation of `pieces`.
+  void slice(const std::vector<HostPiece>& pieces, int64_t b0, int64_t b1) const {
+    int64_t seen = 0;
+    for (const HostPiece& pc : pieces) {
+      if (seen >= b1) break;
+      const int64_t lo = std::max(b0, seen), hi = std::min(b1, seen + pc.len);
+      if (lo < hi) {
+        const int64_t o = pc.off + (lo - seen);
+        uint16_t* o16 = out16 && out16[pc.r] ? static_cast<uint16_t*>(out16[pc.r]) + o : nullptr;
+        cpu_adamw_range(sc, dtype, master[pc.r] + o, m[pc.r] + o, v[pc.r] + o,
+                        grad_shards[pc.r] + o, o16, hi - lo);
+      }
+      seen += pc.len;
+    }
+  }
+};
+
 struct ArgsHolder {
   LaunchArgs* p;
   explicit ArgsHolder(LaunchArgs* q) : p(q) {}
@@ -386,46 +421,27 @@ extern "C" zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* c
   ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
   if (out16_shard) ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, true));
-  const StepScalars sc = make_scalars(*hp, step);
-  // the masked ranks' shards as one list of pieces of at most `chunk` elements
+  const HostUpdate up{make_scalars(*hp, step), dtype, master, m, v, grad_shards, out16_shard};
+  // the masked ranks' shards, concatenated; thread j takes the j-th of nt
+  // equal slices of that concatenation
+  std::vector<HostPiece> pieces;
   int64_t total = 0;
-  for (int r = 0; r < plan->n_ranks; ++r)
-    if (in_mask(rank_mask, r)) total += plan->shard_len[r];
-  int nt = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
-  if (nt < 1) nt = 1;
-  const int64_t chunk = std::max<int64_t>(4096, (total + nt - 1) / nt);
-  struct Piece {
-    int r;
-    int64_t off, len;
-  };
-  std::vector<Piece> pieces;
   try {
     for (int r = 0; r < plan->n_ranks; ++r) {
-      if (!in_mask(rank_mask, r)) continue;
-      for (int64_t off = 0; off < plan->shard_len[r]; off += chunk)
-        pieces.push_back({r, off, std::min(chunk, plan->shard_len[r] - off)});
+      if (!in_mask(rank_mask, r) || plan->shard_len[r] == 0) continue;
+      pieces.push_back({r, 0, plan->shard_len[r]});
+      total += plan->shard_len[r];
     }
   } catch (const std::bad_alloc&) {
     return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
   }
-  auto work = [&](size_t first) {
-    for (size_t j = first; j < pieces.size(); j += static_cast<size_t>(nt)) {
-      const Piece& pc = pieces[j];
-      uint16_t* o = out16_shard && out16_shard[pc.r]
-                        ? static_cast<uint16_t*>(out16_shard[pc.r]) + pc.off
-                        : nullptr;
-      cpu_adamw_range(sc, dtype, master[pc.r] + pc.off, m[pc.r] + pc.off, v[pc.r] + pc.off,
-                      grad_shards[pc.r] + pc.off, o, pc.len);
-    }
-  };
-  nt = static_cast<int>(std::min<size_t>(static_cast<size_t>(nt), pieces.size()));
-  if (nt <= 1) {
-    work(0);
-    return ZERO_OK;
-  }
+  int nt = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+  nt = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({nt, kMaxHostThreads,
+                                                                (total + 4095) / 4096})));
+  auto work = [&](int j) { up.slice(pieces, total * j / nt, total * (j + 1) / nt); };
   std::vector<std::thread> threads;
   try {
-    for (int k = 1; k < nt; ++k) threads.emplace_back(work, static_cast<size_t>(k));
+    for (int j = 1; j < nt; ++j) threads.emplace_back(work, j);
   } catch (const std::exception&) {
     for (auto& th : threads) th.join();
     return fail(ZERO_ERR_OOM, "%s: could not start host threads", fn);
@@ -773,8 +789,10 @@ extern "C" zero_status zero_reduce_scatter_bucket_amp(
 
 namespace {
 
-// Events reused by zero_zero3_pass on this thread (created on first use,
-// timing disabled; never destroyed before the thread exits).
+// Events reused by zero_zero3_pass and zero_offload_step on this thread
+// (created on first use, timing disabled; never destroyed before the thread
+// exits).  Re-recording one is safe: a wait already enqueued on it keeps the
+// record it saw.
 struct EventPool {
   std::vector<cudaEvent_t> ev;
   ~EventPool() {
@@ -782,11 +800,16 @@ struct EventPool {
   }
 };
 
-zero_status pool_events(const char* fn, size_t n, std::vector<cudaEvent_t>** out) {
-  static thread_local EventPool pool;
+// blocking: events whose cudaEventSynchronize puts the host thread to sleep
+// instead of spinning (the offload step's host threads need every core).
+zero_status pool_events(const char* fn, size_t n, std::vector<cudaEvent_t>** out,
+                        bool blocking = false) {
+  static thread_local EventPool spin_pool, block_pool;
+  EventPool& pool = blocking ? block_pool : spin_pool;
   while (pool.ev.size() < n) {
     cudaEvent_t e;
-    const cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    const cudaError_t err = cudaEventCreateWithFlags(
+        &e, cudaEventDisableTiming | (blocking ? cudaEventBlockingSync : 0u));
     if (err != cudaSuccess)
       return fail(ZERO_ERR_CUDA, "%s: cudaEventCreateWithFlags: %s", fn, cudaGetErrorString(err));
     pool.ev.push_back(e);
@@ -869,6 +892,231 @@ extern "C" zero_status zero_zero3_pass(const zero_plan* plan, const zero_layer* 
                        step, all, 0, step_stream));
     if (two) ZERO_TRY(cuda_ok(fn, "cudaEventRecord", cudaEventRecord(released, ss)));
   }
+  return ZERO_OK;
+}
+
+namespace {
+
+// How the offload step may touch a buffer: the device writes the fp32
+// gradient shards and reads the 16-bit shards across the host link, so those
+// must be pinned (or managed) host memory; the host threads read and write
+// master/m/v and both shards, so none of them may be device memory.
+zero_status check_host_buffers(const char* fn, const char* what, void* const* arr,
+                               const zero_plan* plan, uint64_t mask, bool device_accessible) {
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    if (!in_mask(mask, r) || plan->shard_len[r] == 0) continue;
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, arr[r]);
+    if (e != cudaSuccess)
+      return fail(ZERO_ERR_CUDA, "%s: cudaPointerGetAttributes(%s[%d]): %s", fn, what, r,
+                  cudaGetErrorString(e));
+    const bool pinned = at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged;
+    if (device_accessible && !pinned)
+      return fail(ZERO_ERR_INVALID, "%s: %s[%d] must be pinned (or managed) host memory", fn,
+                  what, r);
+    if (at.type == cudaMemoryTypeDevice)
+      return fail(ZERO_ERR_INVALID, "%s: %s[%d] is device memory; the host updates it", fn,
+                  what, r);
+  }
+  return ZERO_OK;
+}
+
+// Launch `kind` over the masked ranks' elements of the flat range [lo, hi),
+// ordered after everything before it on the stream.
+zero_status launch_range(const char* fn, Kind kind, zero_dtype dtype, const zero_plan* plan,
+                         uint64_t mask, int64_t lo, int64_t hi, LaunchArgs& a, void* stream) {
+  std::vector<Job> jobs;
+  build_jobs(plan, mask, lo, hi, jobs);
+  if (jobs.empty()) return ZERO_OK;
+  a.early = 0;
+  return launch_jobs(fn, kind, dtype, a, jobs, stream, nullptr);
+}
+
+// The host side of the offload pipeline: chunk k's update may start once
+// `ready` exceeds k; each worker counts itself into done[k] when its share of
+// chunk k is written.
+struct OffloadSync {
+  std::mutex mu;
+  std::condition_variable ready_cv, done_cv;
+  int64_t ready = 0;
+  bool abort = false;
+  std::vector<int> done;
+};
+
+}  // namespace
+
+extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* const* grads,
+                                         zero_dtype dtype, zero_reduce_op op,
+                                         float* const* grad_shards, float* const* master,
+                                         float* const* m, float* const* v,
+                                         void* const* out16_shard, void* full_flat16,
+                                         const zero_adamw_hparams* hp, int64_t step,
+                                         uint64_t rank_mask, int64_t chunk_elems,
+                                         int32_t n_threads, void* stream) {
+  const char* fn = "zero_offload_step";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, step));
+  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
+  ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, false));
+  if (full_flat16 && !aligned16(full_flat16))
+    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  const int64_t total = plan->padded;
+  const int64_t C = chunk_elems > 0 ? chunk_elems : std::max<int64_t>(total, 1);
+  const int64_t K = (total + C - 1) / C;
+  if (K > kMaxOffloadChunks)
+    return fail(ZERO_ERR_INVALID, "%s: %" PRId64 " chunks of %" PRId64 " elements; at most %d",
+                fn, K, C, kMaxOffloadChunks);
+  ZERO_TRY(pending_error(fn));
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  ZERO_TRY(cuda_ok(fn, "cudaStreamIsCapturing",
+                   cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap)));
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(ZERO_ERR_UNSUPPORTED, "%s: cannot be captured: the host waits for the device", fn);
+  ZERO_TRY(check_host_buffers(fn, "grad_shards", reinterpret_cast<void* const*>(grad_shards),
+                              plan, rank_mask, true));
+  ZERO_TRY(check_host_buffers(fn, "out16_shard", out16_shard, plan, rank_mask, true));
+  ZERO_TRY(check_host_buffers(fn, "master", reinterpret_cast<void* const*>(master), plan,
+                              rank_mask, false));
+  ZERO_TRY(check_host_buffers(fn, "m", reinterpret_cast<void* const*>(m), plan, rank_mask, false));
+  ZERO_TRY(check_host_buffers(fn, "v", reinterpret_cast<void* const*>(v), plan, rank_mask, false));
+  if (K == 0) return ZERO_OK;
+
+  // each chunk's host pieces: the masked ranks' runs cut to the chunk
+  std::vector<std::vector<HostPiece>> pieces;
+  std::vector<int64_t> chunk_len;
+  try {
+    pieces.resize(static_cast<size_t>(K));
+    chunk_len.assign(static_cast<size_t>(K), 0);
+    for (int64_t k = 0; k < K; ++k) {
+      const int64_t lo = k * C, hi = std::min(total, lo + C);
+      for (int r = 0; r < plan->n_ranks; ++r) {
+        if (!in_mask(rank_mask, r)) continue;
+        for (const auto& run : plan->runs[r]) {
+          const int64_t a = std::max(lo, run.flat_off);
+          const int64_t b = std::min(hi, run.flat_off + run.len);
+          if (a >= b) continue;
+          pieces[k].push_back({r, run.shard_off + (a - run.flat_off), b - a});
+          chunk_len[k] += b - a;
+        }
+      }
+    }
+  } catch (const std::bad_alloc&) {
+    return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  }
+
+  ArgsHolder red(new_args()), gat(new_args());
+  if (!red.p || !gat.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    red.p->grads[r] = grads[r];
+    if (!in_mask(rank_mask, r)) continue;
+    red.p->gshard[r] = grad_shards[r];
+    gat.p->shard16[r] = out16_shard[r];
+  }
+  set_scale(*red.p, plan->n_ranks, op);
+  set_bounds(*red.p, plan);
+  gat.p->full16 = full_flat16;
+  set_bounds(*gat.p, plan);
+
+  // 1. every chunk's reduction, each followed by its event
+  std::vector<cudaEvent_t>* ev = nullptr;
+  ZERO_TRY(pool_events(fn, static_cast<size_t>(K), &ev, true));
+  for (int64_t k = 0; k < K; ++k) {
+    const int64_t lo = k * C, hi = std::min(total, lo + C);
+    ZERO_TRY(launch_range(fn, Kind::kReduceScatter, dtype, plan, rank_mask, lo, hi, *red.p,
+                          stream));
+    ZERO_TRY(cuda_ok(fn, "cudaEventRecord",
+                     cudaEventRecord((*ev)[k], static_cast<cudaStream_t>(stream))));
+  }
+
+  // 2. host workers: worker j updates the j-th of nt equal slices of each
+  //    chunk as soon as that chunk's reduction has completed
+  const HostUpdate up{make_scalars(*hp, step), dtype, master, m, v, grad_shards, out16_shard};
+  // the calling thread waits for the device and launches the gathers, so by
+  // default one hardware thread is left to it
+  int nt = n_threads > 0 ? n_threads
+                         : static_cast<int>(std::thread::hardware_concurrency()) - 1;
+  nt = std::max(1, std::min(nt, kMaxHostThreads));
+  OffloadSync sync;
+  try {
+    sync.done.assign(static_cast<size_t>(K), 0);
+  } catch (const std::bad_alloc&) {
+    return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  }
+  auto worker = [&](int j) {
+    for (int64_t k = 0; k < K; ++k) {
+      {
+        std::unique_lock<std::mutex> lk(sync.mu);
+        sync.ready_cv.wait(lk, [&] { return sync.ready > k || sync.abort; });
+        if (sync.abort) return;
+      }
+      const int64_t T = chunk_len[k];
+      up.slice(pieces[k], T * j / nt, T * (j + 1) / nt);
+      std::lock_guard<std::mutex> lk(sync.mu);
+      if (++sync.done[k] == nt) sync.done_cv.notify_all();
+    }
+  };
+  std::vector<std::thread> threads;
+  auto stop = [&](zero_status st) {
+    {
+      std::lock_guard<std::mutex> lk(sync.mu);
+      sync.abort = true;
+    }
+    sync.ready_cv.notify_all();
+    for (auto& th : threads) th.join();
+    return st;
+  };
+  try {
+    for (int j = 0; j < nt; ++j) threads.emplace_back(worker, j);
+  } catch (const std::exception&) {
+    return stop(fail(ZERO_ERR_OOM, "%s: could not start host threads", fn));
+  }
+
+  // 3. release each chunk to the workers when its reduction is done; gather
+  //    every chunk the workers have finished, as soon as it is finished
+  int64_t gathered = 0;
+  auto gather_finished = [&](bool wait_all) -> zero_status {
+    while (gathered < K) {
+      {
+        std::unique_lock<std::mutex> lk(sync.mu);
+        if (wait_all)
+          sync.done_cv.wait(lk, [&] { return sync.done[gathered] == nt; });
+        else if (sync.done[gathered] != nt)
+          return ZERO_OK;
+      }
+      const int64_t lo = gathered * C, hi = std::min(total, lo + C);
+      if (full_flat16) {
+        const zero_status st = launch_range(fn, Kind::kAllgather, dtype, plan, rank_mask, lo,
+                                            hi, *gat.p, stream);
+        if (st != ZERO_OK) return st;
+      }
+      ++gathered;
+    }
+    return ZERO_OK;
+  };
+  for (int64_t k = 0; k < K; ++k) {
+    const cudaError_t e = cudaEventSynchronize((*ev)[k]);
+    if (e != cudaSuccess)
+      return stop(fail(ZERO_ERR_CUDA, "%s: reduction of chunk %" PRId64 ": %s", fn, k,
+                       cudaGetErrorString(e)));
+    {
+      std::lock_guard<std::mutex> lk(sync.mu);
+      sync.ready = k + 1;
+    }
+    sync.ready_cv.notify_all();
+    const zero_status st = gather_finished(false);
+    if (st != ZERO_OK) return stop(st);
+  }
+  const zero_status st = gather_finished(true);
+  if (st != ZERO_OK) return stop(st);
+  for (auto& th : threads) th.join();
   return ZERO_OK;
 }
 

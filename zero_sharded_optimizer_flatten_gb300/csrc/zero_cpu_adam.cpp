@@ -1,8 +1,11 @@
 // Host-side AdamW of the offloaded optimizer (ZeRO-Offload's CPU optimizer):
-// the element loop the host threads of zero_cpu_adamw_shard_step run.  It
-// performs the same binary32 operations in the same order as the GPU update
-// (compiled with -ffp-contract=off, so no operation is fused into an FMA;
-// division and square root are the IEEE ones), so both give identical bits.
+// the element loop the host threads of zero_cpu_adamw_shard_step and
+// zero_offload_step run.  It performs the same binary32 operations in the
+// same order as the GPU update (compiled with -ffp-contract=off, so no
+// operation is fused into an FMA; division and square root are the IEEE
+// ones), so both give identical bits.  The 16-bit cast is made in the same
+// pass, while the updated value is still in a register: the loop streams
+// 16 bytes in and 12 + 2 out per element, once.
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -13,13 +16,14 @@ namespace zero {
 namespace {
 
 // Round to nearest even on the upper half of the binary32 pattern; NaN stays
-// a quiet NaN with its sign.
+// a quiet NaN with its sign.  Written without a branch so that the loop
+// below stays vectorisable.
 inline uint16_t to_bf16(float x) {
   uint32_t u;
   memcpy(&u, &x, 4);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x0040u);
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return static_cast<uint16_t>(u >> 16);
+  const uint32_t rounded = (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+  const uint32_t quiet = (u >> 16) | 0x0040u;
+  return static_cast<uint16_t>((u & 0x7fffffffu) > 0x7f800000u ? quiet : rounded);
 }
 
 inline uint16_t to_fp16(float x) {
@@ -29,11 +33,12 @@ inline uint16_t to_fp16(float x) {
   return r;
 }
 
-}  // namespace
+enum Cast { kNoCast, kCastBf16, kCastFp16 };
 
-void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* __restrict p,
-                     float* __restrict m, float* __restrict v, const float* __restrict g,
-                     uint16_t* __restrict out16, int64_t n) {
+template <Cast C>
+void adamw_loop(const StepScalars& s, float* __restrict p, float* __restrict m,
+                float* __restrict v, const float* __restrict g, uint16_t* __restrict out16,
+                int64_t n) {
   for (int64_t i = 0; i < n; ++i) {
     const float gi = g[i];
     float pp = p[i] * s.d;
@@ -44,13 +49,21 @@ void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* __restrict p
     p[i] = pp;
     m[i] = mm;
     v[i] = vv;
+    if (C == kCastBf16) out16[i] = to_bf16(pp);
+    if (C == kCastFp16) out16[i] = to_fp16(pp);
   }
-  if (!out16) return;
-  if (dtype == ZERO_BF16) {
-    for (int64_t i = 0; i < n; ++i) out16[i] = to_bf16(p[i]);
-  } else {
-    for (int64_t i = 0; i < n; ++i) out16[i] = to_fp16(p[i]);
-  }
+}
+
+}  // namespace
+
+void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m, float* v,
+                     const float* g, uint16_t* out16, int64_t n) {
+  if (!out16)
+    adamw_loop<kNoCast>(s, p, m, v, g, nullptr, n);
+  else if (dtype == ZERO_BF16)
+    adamw_loop<kCastBf16>(s, p, m, v, g, out16, n);
+  else
+    adamw_loop<kCastFp16>(s, p, m, v, g, out16, n);
 }
 
 }  // namespace zero

@@ -94,6 +94,8 @@ def lib():
                                               i64, vp],
                 "zero_cpu_adamw_shard_step": [vp, vpp, vpp, vpp, vpp, vpp, ctypes.c_int, hp, i64,
                                               u64, i32],
+                "zero_offload_step": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp,
+                                      vpp, vp, hp, i64, u64, i64, i32, vp],
                 "zero_amp_init": [vp, ctypes.POINTER(AmpConfigC), vp],
                 "zero_amp_workspace_bytes": [vp, u64, i64, i64p],
                 "zero_step_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp, vp,
@@ -841,39 +843,70 @@ def _host_addr(a, what):
     raise TypeError(f"{what}: expected a numpy array, a host tensor or an int address")
 
 
+def _host_per_rank(plan: Plan, seq, what: str, mask: int, nullable: bool = False):
+    """Pointer array of per-rank host arrays (entries of unmasked ranks, and
+    None entries when nullable, become NULL); None -> NULL array."""
+    if seq is None:
+        return None
+    if len(seq) != plan.n_ranks:
+        raise ValueError(f"{what}: expected {plan.n_ranks} entries")
+    vals = []
+    for r, a in enumerate(seq):
+        if not (mask >> r) & 1 or (a is None and nullable):
+            vals.append(0)
+            continue
+        n = a.size if isinstance(a, np.ndarray) else (a.numel() if hasattr(a, "numel") else None)
+        if n is not None and n < plan.shard_len(r):
+            raise ValueError(f"{what}[{r}]: {n} elements, needs {plan.shard_len(r)}")
+        vals.append(_host_addr(a, f"{what}[{r}]"))
+    return _ptrs(vals)
+
+
 def zero_cpu_adamw_shard_step(plan: Plan, master, m, v, grad_shards, out16_shard, hparams: AdamW,
                               step: int, dtype: int, rank_mask=None, n_threads: int = 0):
     """ZeRO-Offload's CPU optimizer: AdamW + cast by host threads on host
     buffers (lists of n_ranks host arrays; entries of unmasked ranks ignored)."""
-    L = lib()
-    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
-    L.zero_cpu_adamw_shard_step.argtypes = [vp, vpp, vpp, vpp, vpp, vpp, ctypes.c_int,
-                                            ctypes.POINTER(AdamWHparams), ctypes.c_int64,
-                                            ctypes.c_uint64, ctypes.c_int32]
-    L.zero_cpu_adamw_shard_step.restype = ctypes.c_int
     mask = _mask(plan, rank_mask)
 
     def arr(seq, what, nullable=False):
-        if seq is None:
-            return None
-        if len(seq) != plan.n_ranks:
-            raise ValueError(f"{what}: expected {plan.n_ranks} entries")
-        vals = []
-        for r, a in enumerate(seq):
-            if not (mask >> r) & 1 or (a is None and nullable):
-                vals.append(0)
-                continue
-            n = a.size if isinstance(a, np.ndarray) else (a.numel() if hasattr(a, "numel") else None)
-            if n is not None and n < plan.shard_len(r):
-                raise ValueError(f"{what}[{r}]: {n} elements, needs {plan.shard_len(r)}")
-            vals.append(_host_addr(a, f"{what}[{r}]"))
-        return _ptrs(vals)
+        return _host_per_rank(plan, seq, what, mask, nullable)
     hp = hparams.c()
     o16 = arr(out16_shard, "out16_shard", nullable=True)
-    _check(L.zero_cpu_adamw_shard_step(plan.handle, arr(master, "master"), arr(m, "m"),
-                                       arr(v, "v"), arr(grad_shards, "grad_shards"), o16,
-                                       int(dtype), ctypes.byref(hp), int(step), mask,
-                                       int(n_threads)))
+    _check(lib().zero_cpu_adamw_shard_step(plan.handle, arr(master, "master"), arr(m, "m"),
+                                           arr(v, "v"), arr(grad_shards, "grad_shards"), o16,
+                                           int(dtype), ctypes.byref(hp), int(step), mask,
+                                           int(n_threads)))
+
+
+def zero_offload_step(plan: Plan, grads, op, grad_shards, master, m, v, out16_shard,
+                      full_flat16, hparams: AdamW, step: int, rank_mask=None,
+                      chunk_elems: Optional[int] = None, n_threads: int = 0, stream=None,
+                      dtype=None):
+    """ZeRO-Offload with the CPU optimizer, pipelined over chunks of the flat
+    buffer (see zero.h): device reduce-scatter into the pinned host
+    grad_shards, host AdamW + cast on the host master/m/v into the pinned
+    host out16_shard, device all-gather into full_flat16 (device, or None).
+    chunk_elems None: the flat buffer in 8 chunks; 0: one chunk."""
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    if len(grads) != plan.n_ranks:
+        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    o16 = _per_rank(plan, out16_shard, "out16_shard", mask)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    if chunk_elems is None:
+        chunk_elems = max(1, -(-plan.padded // 8))
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    hp = hparams.c()
+    _check(lib().zero_offload_step(plan.handle, _ptrs(g), dt, op_i, _ptrs(gs),
+                                   _host_per_rank(plan, master, "master", mask),
+                                   _host_per_rank(plan, m, "m", mask),
+                                   _host_per_rank(plan, v, "v", mask),
+                                   _ptrs(o16), full, ctypes.byref(hp), int(step), mask,
+                                   int(chunk_elems), int(n_threads), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------
