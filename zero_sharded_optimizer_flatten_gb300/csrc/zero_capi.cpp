@@ -24,6 +24,9 @@
 
 namespace zero {
 
+constexpr int kMaxHostThreads = 1024;    // host threads of one host optimizer call
+constexpr int kMaxOffloadChunks = 4096;  // chunks (one event each) of one offload step
+
 char* error_buffer() {
   static thread_local char buf[1024];
   return buf;

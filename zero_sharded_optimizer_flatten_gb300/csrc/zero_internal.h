@@ -20,8 +20,6 @@ constexpr int kVec = 4;           // elements per quad (8 B of 16-bit, 16 B of f
 constexpr int kHalf = kThreads * kVec;  // 1024: distance between a thread's two quads
 constexpr int kTile = 2 * kHalf;  // 2048 elements per CTA per tile
 constexpr int kMaxJobs = 192;     // jobs carried in one launch's parameters
-constexpr int kMaxHostThreads = 1024;    // host threads of one offload call
-constexpr int kMaxOffloadChunks = 4096;  // chunks (one event each) of one offload step
 
 // Resident CTAs per SM the kernels are compiled for (caps registers at 64),
 // and the grid: ZERO_GRID_MULT = 0 launches one CTA per tile; k > 0 caps the
@@ -173,8 +171,7 @@ struct AmpParams {
 // The binary32 constants of step t (zero_capi.cpp).
 StepScalars make_scalars(const zero_adamw_hparams& h, int64_t t);
 
-// AdamW + cast over n elements of host memory (zero_cpu_adam.cpp); out16
-// may be NULL (no cast).
+// AdamW + cast over n elements of host memory (zero_cpu_adam.cpp).
 void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m, float* v,
                      const float* g, uint16_t* out16, int64_t n);
 
