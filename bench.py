@@ -1298,7 +1298,8 @@ def run_engine(args, world, rank, local):
     for overlap in (False, True):
         model = toy()
         eng = ZeroEngine(model.parameters(), N, mode="round_robin", op="sum",
-                         bucket_elems=args.bucket, overlap_comm=overlap, amp=amp)
+                         bucket_elems=args.bucket, overlap_comm=overlap, amp=amp,
+                         offload=args.engine_offload, host_threads=args.threads)
 
         def iteration():
             for q in range(N):
@@ -1324,7 +1325,9 @@ def run_engine(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": "ToyModel hidden 1024 x12 + Linear(1024,10), round-robin N=4"
-                                   + (", mixed precision (loss scale, clipping)" if amp else ""),
+                                   + (", mixed precision (loss scale, clipping)" if amp else "")
+                                   + (f", optimizer offload {args.engine_offload}"
+                                      if args.engine_offload else ""),
                        "phi": phi, "tokens_per_rank": args.tokens, "bucket_elems": args.bucket,
                        "ms_per_iteration": {"serial": out["serial"], "overlap": out["overlap"]},
                        "bucket_launches_during_backward": out["launched_during_backward"]}}
@@ -1392,6 +1395,9 @@ def main(argv=None):
     ap.add_argument("--engine", action="store_true",
                     help="time a training iteration through the autograd-driven engine")
     ap.add_argument("--tokens", type=int, default=4096, help="--engine: tokens per rank")
+    ap.add_argument("--engine-offload", choices=["cpu", "host_state"], default=None,
+                    help="--engine: optimizer state in pinned host memory (cpu: host AdamW; "
+                         "host_state: GPU AdamW across the host link)")
     ap.add_argument("--bucket", type=int, default=5_000_000, help="--engine: bucket elements")
     ap.add_argument("--layer-states", type=int, default=40,
                     help="ZeRO-3 stream: distinct layer states kept (cycled if fewer than layers)")

@@ -126,3 +126,64 @@ def test_engine_requires_every_rank():
         eng.step()
     with pytest.raises(RuntimeError):
         eng.backward(_loss(model, _batch(0, 1, torch.bfloat16)), 0)
+
+
+@pytest.mark.parametrize("offload,overlap,dtype", [("cpu", True, torch.bfloat16),
+                                                   ("cpu", False, torch.float16),
+                                                   ("host_state", True, torch.bfloat16)])
+def test_engine_offload_modes_equal_the_device_engine(offload, overlap, dtype):
+    """offload_optimizer to the host: the CPU optimizer (reductions into pinned
+    host shards, host AdamW + cast, gather) and the host-resident state that
+    the GPU kernels update across the link both give the device engine's
+    parameters and state bit for bit."""
+    a, b = _mlp(dtype), _mlp(dtype)
+    ea = ZeroEngine(a.parameters(), 4, bucket_elems=60_000, overlap_comm=overlap)
+    eb = ZeroEngine(b.parameters(), 4, bucket_elems=60_000, overlap_comm=overlap,
+                    offload=offload, host_threads=3)
+    assert all(not x.is_cuda and x.is_pinned() for x in eb.master + eb.m + eb.v)
+    if offload == "cpu":
+        assert all(x.is_pinned() for x in eb.grad_shards + eb.shard16)
+    for t in (1, 2, 3):
+        for q in range(4):
+            x = _batch(q, t, dtype)
+            ea.backward(_loss(a, x), q)
+            eb.backward(_loss(b, x), q)
+        ea.step()
+        eb.step()
+    torch.cuda.synchronize()
+    assert torch.equal(ea.flat16, eb.flat16)
+    for r in range(4):
+        for xa, xb in ((ea.master[r], eb.master[r]), (ea.m[r], eb.m[r]), (ea.v[r], eb.v[r])):
+            assert torch.equal(xa.cpu(), xb.cpu())
+
+
+def test_engine_mixed_precision_with_host_resident_state():
+    """amp with the state in host memory: the same device decisions and
+    updates as the device-resident engine, bit for bit (fp16, a loss scale
+    that overflows at first, clipping)."""
+    cfg = Z.AmpConfig(init_scale=2.0 ** 24, min_scale=1.0, window=20, hysteresis=1,
+                      max_norm=1.0)
+    a, b = _mlp(torch.float16), _mlp(torch.float16)
+    ea = ZeroEngine(a.parameters(), 4, bucket_elems=60_000, amp=cfg)
+    eb = ZeroEngine(b.parameters(), 4, bucket_elems=60_000, amp=cfg, offload="host_state")
+    for t in range(1, 8):
+        for q in range(4):
+            x = _batch(q, t, torch.float16)
+            ea.backward(_loss(a, x), q)
+            eb.backward(_loss(b, x), q)
+        ea.step()
+        eb.step()
+    torch.cuda.synchronize()
+    sa, sb = ea.amp_status(), eb.amp_status()
+    assert bytes(sa) == bytes(sb) and sa.skipped >= 1
+    assert torch.equal(ea.flat16, eb.flat16)
+    for r in range(4):
+        assert torch.equal(ea.master[r].cpu(), eb.master[r])
+        assert torch.equal(ea.v[r].cpu(), eb.v[r])
+
+
+def test_engine_offload_arguments():
+    with pytest.raises(ValueError):
+        ZeroEngine(_mlp(torch.bfloat16).parameters(), 2, offload="nvme")
+    with pytest.raises(ValueError):
+        ZeroEngine(_mlp(torch.float16).parameters(), 2, offload="cpu", amp=Z.AmpConfig())

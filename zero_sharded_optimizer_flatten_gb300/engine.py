@@ -28,6 +28,17 @@ skip, scale update, clipping, AdamW, cast, gather;
 ``zero_step_amp_reduced``), bit-identical to ``zero_step_amp`` on the
 replicas with the same bucket size.
 
+With ``offload`` the fp32 optimizer state lives in pinned host memory, as
+the pages' ds_config ``offload_optimizer: {device: cpu, pin_memory: true}``
+asks ("DeepSpeed ZeRO-2 ..." §4.5).  ``offload="cpu"`` is that form: the
+bucket reductions write the fp32 gradient shards into pinned host memory
+across the host link, ``step()`` runs AdamW + cast on host threads
+(``zero_cpu_adamw_shard_step``) and all-gathers the host 16-bit shards.
+``offload="host_state"`` keeps the update on the GPU, whose kernels read and
+write the host-resident master/m/v across NVLink-C2C (no host
+synchronisation; works with ``amp`` too).  Both give the device engine's
+results bit for bit.
+
 The arithmetic is the library's (no compute happens here); this module only
 does bookkeeping and launches.
 """
@@ -44,7 +55,8 @@ class ZeroEngine:
     def __init__(self, params: Iterable[torch.nn.Parameter], n_ranks: int, *, mode="flat",
                  align: int = 16, op: str = "avg", hparams: Optional[Z.AdamW] = None,
                  bucket_elems: int = 50_000_000, overlap_comm: bool = True,
-                 amp: Optional[Z.AmpConfig] = None):
+                 amp: Optional[Z.AmpConfig] = None, offload: Optional[str] = None,
+                 host_threads: int = 0):
         self.params: List[torch.nn.Parameter] = list(params)
         if not self.params:
             raise ValueError("no parameters")
@@ -55,6 +67,12 @@ class ZeroEngine:
         for p in self.params:
             if p.dtype != dt or p.device != dev or not p.is_cuda:
                 raise ValueError("all parameters must share one 16-bit dtype and one CUDA device")
+        if offload not in (None, "cpu", "host_state"):
+            raise ValueError("offload must be None, 'cpu' or 'host_state'")
+        if offload == "cpu" and amp is not None:
+            raise ValueError("the CPU optimizer has no mixed-precision controls; use "
+                             "offload='host_state' with amp")
+        self.offload, self.host_threads = offload, host_threads
         self.n_ranks, self.op = n_ranks, op
         self.hp = hparams or Z.AdamW()
         self.numel = [p.numel() for p in self.params]
@@ -72,11 +90,19 @@ class ZeroEngine:
         # per-rank gradient replicas, fp32 gradient shards, optimizer state
         self.grads = [torch.zeros(P, dtype=dt, device=dev) for _ in range(n_ranks)]
         S = [plan.shard_len(r) for r in range(n_ranks)]
-        self.grad_shards = [torch.zeros(n, dtype=torch.float32, device=dev) for n in S]
-        self.master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
-        self.m = [torch.empty_like(x) for x in self.master]
-        self.v = [torch.empty_like(x) for x in self.master]
-        self.shard16 = [torch.empty(n, dtype=dt, device=dev) for n in S]
+
+        def shard_buf(n, dtype, on_host):
+            if on_host:
+                return torch.zeros(n, dtype=dtype, pin_memory=True)
+            return torch.zeros(n, dtype=dtype, device=dev)
+        host = offload == "cpu"
+        self.grad_shards = [shard_buf(n, torch.float32, host) for n in S]
+        self.master = [shard_buf(n, torch.float32, offload is not None) for n in S]
+        self.m = [shard_buf(n, torch.float32, offload is not None) for n in S]
+        self.v = [shard_buf(n, torch.float32, offload is not None) for n in S]
+        self.shard16 = [shard_buf(n, dt, host) for n in S]
+        # master = the 16-bit values widened, m = v = 0 (the kernel writes
+        # host-resident state across the link as well)
         Z.zero_init_shards(plan, self.flat16, self.master, self.m, self.v)
         # buckets over the flat index space; the tail padding needs no filling
         B = bucket_elems if bucket_elems > 0 else P
@@ -191,6 +217,14 @@ class ZeroEngine:
             Z.zero_step_amp_reduced(self.plan, self.grad_shards, self.master, self.m, self.v,
                                     self.flat16, None, self.hp, self.amp, self.amp_state,
                                     self._workspace, bucket_elems=self.bucket_elems)
+        elif self.offload == "cpu":
+            # the host update reads the reduced gradients the device wrote
+            torch.cuda.current_stream().synchronize()
+            dt = Z.ZERO_BF16 if self.flat16.dtype == torch.bfloat16 else Z.ZERO_FP16
+            Z.zero_cpu_adamw_shard_step(self.plan, self.master, self.m, self.v,
+                                        self.grad_shards, self.shard16, self.hp, self.step_count,
+                                        dt, n_threads=self.host_threads)
+            Z.zero_allgather(self.plan, self.shard16, self.flat16)
         else:
             Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
                                     self.shard16, self.hp, self.step_count)
