@@ -12,7 +12,9 @@
  * Grace-Blackwell), which replaces an explicit copy; they run at the link's
  * bandwidth instead of HBM's.  Every stream argument is a cudaStream_t passed
  * as void* (NULL = the legacy default stream).  Compute calls are
- * asynchronous on that stream.
+ * asynchronous on that stream, except the two that run the optimizer on
+ * host threads (zero_cpu_adamw_shard_step, zero_offload_step), which return
+ * when the host work is done.
  *
  * Sources (page title, section) for what each call computes:
  *  [ZeRO-2 blog]   "DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com):
