@@ -621,6 +621,31 @@ def test_pipelined_offload_step(numel, N, mode, dtype, op, mask, chunk, threads)
     assert not u16(full)[~owned].any(), "an unmasked rank's elements were written"
 
 
+def test_pipelined_offload_step_edge_cases():
+    """A group without elements (nothing launched), no gathered buffer (the
+    host 16-bit shards are still written) and a chunk larger than the flat
+    buffer (one chunk)."""
+    plan = Z.zero_plan_partitions([0, 0], 2, "flat", 16)
+    empty16 = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    null = [0, 0]          # empty shards need no buffer (NULL addresses)
+    before = Z.zero_launch_count()
+    Z.zero_offload_step(plan, [empty16] * 2, "avg", null, null, null, null, null, empty16, HP, 1,
+                        dtype=Z.ZERO_BF16)
+    assert Z.zero_launch_count() == before
+    w = W.small((30000, 37), 2, mode="flat", align=16, dtype="bf16", op="avg")
+    c = Case(w)
+    hm, hmm, hv, hg, h16 = _host_offload_state(c)
+    for t in (1, 2):
+        g = c.grads(t)
+        Z.zero_offload_step(c.plan, g, "avg", hg, hm, hmm, hv, h16, None, HP, t,
+                            chunk_elems=10 ** 9)
+        Z.zero_step(c.plan, g, "avg", c.master, c.m, c.v, c.full16, None, HP, t)
+    torch.cuda.synchronize()
+    for r in range(2):
+        assert torch.equal(hm[r], c.master[r].cpu())
+        off = c.plan.shards[r][0]
+        assert torch.equal(h16[r], c.full16[off:off + c.plan.shard_len(r)].cpu())
+
 def test_pipelined_offload_step_rejects_bad_arguments_without_launching():
     w = W.small((30000, 37), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = Case(w, with_oracle=False)
