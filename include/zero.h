@@ -254,7 +254,11 @@ zero_status zero_cpu_adamw_shard_step(const zero_plan* plan, float* const* maste
  * host threads update chunk k as soon as its reduction has completed (while
  * the device still reduces the chunks after it), and chunk k's all-gather is
  * enqueued as soon as the host has written its 16-bit values.
- *  grads: the N flat replicas (device, or pinned host memory).
+ *  grads: the N flat replicas (device, or pinned host memory); or NULL when
+ *    grad_shards already hold the reduced gradients (reduced bucket by bucket
+ *    during backward): then nothing is reduced, `op` is not used, and the
+ *    host update starts once the work enqueued on `stream` before the call
+ *    has completed (the update and the gathers still overlap).
  *  grad_shards, out16_shard: PINNED (or managed) host memory the device
  *    writes (fp32 reduced gradient) and reads (16-bit shard) across the host
  *    link; checked with cudaPointerGetAttributes (ZERO_ERR_INVALID otherwise).

@@ -646,6 +646,33 @@ def test_pipelined_offload_step_edge_cases():
         off = c.plan.shards[r][0]
         assert torch.equal(h16[r], c.full16[off:off + c.plan.shard_len(r)].cpu())
 
+@pytest.mark.parametrize("chunk", [None, 0, 777])
+def test_offload_step_from_reduced_shards(chunk):
+    """grads=None: the gradient shards were reduced before the call (here by
+    zero_reduce_scatter on the same stream, with no synchronisation in
+    between); the step waits for that work, updates on the host and
+    gathers, bit for bit like the serial calls."""
+    w = W.small((30000, 37, 4096), 4, mode="round_robin", align=16, dtype="fp16", op="sum")
+    c = Case(w, with_oracle=False)
+    hm, hmm, hv, hg, h16 = _host_offload_state(c)
+    sm, smm, sv, sg, s16 = _host_offload_state(c)
+    full = torch.zeros_like(c.full16)
+    sfull = torch.zeros_like(c.full16)
+    for t in (1, 2):
+        g = c.grads(t)
+        Z.zero_reduce_scatter(c.plan, g, "sum", hg)
+        Z.zero_offload_step(c.plan, None, "sum", hg, hm, hmm, hv, h16, full, HP, t,
+                            chunk_elems=chunk, n_threads=3)
+        Z.zero_reduce_scatter(c.plan, g, "sum", sg)
+        Z.zero_sync()
+        Z.zero_cpu_adamw_shard_step(c.plan, sm, smm, sv, sg, s16, HP, t, Z.ZERO_FP16)
+        Z.zero_allgather(c.plan, s16, sfull)
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert torch.equal(hm[r], sm[r]) and torch.equal(hv[r], sv[r])
+        assert torch.equal(h16[r], s16[r])
+    assert torch.equal(full, sfull)
+
 def test_pipelined_offload_step_rejects_bad_arguments_without_launching():
     w = W.small((30000, 37), 2, mode="flat", align=16, dtype="bf16", op="avg")
     c = Case(w, with_oracle=False)

@@ -963,7 +963,7 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   ZERO_TRY(check_dtype(fn, dtype));
   if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
   ZERO_TRY(check_hparams(fn, hp, step));
-  ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  if (grads) ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
   ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
   ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
@@ -1018,7 +1018,7 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   ArgsHolder red(new_args()), gat(new_args());
   if (!red.p || !gat.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
   for (int r = 0; r < plan->n_ranks; ++r) {
-    red.p->grads[r] = grads[r];
+    red.p->grads[r] = grads ? grads[r] : nullptr;
     if (!in_mask(rank_mask, r)) continue;
     red.p->gshard[r] = grad_shards[r];
     gat.p->shard16[r] = out16_shard[r];
@@ -1028,13 +1028,18 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   gat.p->full16 = full_flat16;
   set_bounds(*gat.p, plan);
 
-  // 1. every chunk's reduction, each followed by its event
+  // 1. every chunk's reduction, each followed by its event; without grads
+  //    (the shards already hold the reduced gradients) one event marks the
+  //    end of the work enqueued on the stream before the call
   std::vector<cudaEvent_t>* ev = nullptr;
-  ZERO_TRY(pool_events(fn, static_cast<size_t>(K), &ev, true));
-  for (int64_t k = 0; k < K; ++k) {
-    const int64_t lo = k * C, hi = std::min(total, lo + C);
-    ZERO_TRY(launch_range(fn, Kind::kReduceScatter, dtype, plan, rank_mask, lo, hi, *red.p,
-                          stream));
+  const int64_t n_events = grads ? K : 1;
+  ZERO_TRY(pool_events(fn, static_cast<size_t>(n_events), &ev, true));
+  for (int64_t k = 0; k < n_events; ++k) {
+    if (grads) {
+      const int64_t lo = k * C, hi = std::min(total, lo + C);
+      ZERO_TRY(launch_range(fn, Kind::kReduceScatter, dtype, plan, rank_mask, lo, hi, *red.p,
+                            stream));
+    }
     ZERO_TRY(cuda_ok(fn, "cudaEventRecord",
                      cudaEventRecord((*ev)[k], static_cast<cudaStream_t>(stream))));
   }
@@ -1104,14 +1109,14 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
     }
     return ZERO_OK;
   };
-  for (int64_t k = 0; k < K; ++k) {
+  for (int64_t k = 0; k < n_events; ++k) {
     const cudaError_t e = cudaEventSynchronize((*ev)[k]);
     if (e != cudaSuccess)
       return stop(fail(ZERO_ERR_CUDA, "%s: reduction of chunk %" PRId64 ": %s", fn, k,
                        cudaGetErrorString(e)));
     {
       std::lock_guard<std::mutex> lk(sync.mu);
-      sync.ready = k + 1;
+      sync.ready = grads ? k + 1 : K;
     }
     sync.ready_cv.notify_all();
     const zero_status st = gather_finished(false);

@@ -32,8 +32,9 @@ With ``offload`` the fp32 optimizer state lives in pinned host memory, as
 the pages' ds_config ``offload_optimizer: {device: cpu, pin_memory: true}``
 asks ("DeepSpeed ZeRO-2 ..." §4.5).  ``offload="cpu"`` is that form: the
 bucket reductions write the fp32 gradient shards into pinned host memory
-across the host link, ``step()`` runs AdamW + cast on host threads
-(``zero_cpu_adamw_shard_step``) and all-gathers the host 16-bit shards.
+across the host link, ``step()`` runs AdamW + cast on host threads and
+all-gathers the host 16-bit shards, chunk by chunk so that the gathers
+overlap the update (``zero_offload_step`` on the reduced shards).
 ``offload="host_state"`` keeps the update on the GPU, whose kernels read and
 write the host-resident master/m/v across NVLink-C2C (no host
 synchronisation; works with ``amp`` too).  Both give the device engine's
@@ -218,13 +219,12 @@ class ZeroEngine:
                                     self.flat16, None, self.hp, self.amp, self.amp_state,
                                     self._workspace, bucket_elems=self.bucket_elems)
         elif self.offload == "cpu":
-            # the host update reads the reduced gradients the device wrote
-            torch.cuda.current_stream().synchronize()
-            dt = Z.ZERO_BF16 if self.flat16.dtype == torch.bfloat16 else Z.ZERO_FP16
-            Z.zero_cpu_adamw_shard_step(self.plan, self.master, self.m, self.v,
-                                        self.grad_shards, self.shard16, self.hp, self.step_count,
-                                        dt, n_threads=self.host_threads)
-            Z.zero_allgather(self.plan, self.shard16, self.flat16)
+            # the gradient shards are reduced already: the host update waits
+            # for the stream, and each chunk's gather overlaps the next
+            # chunk's update
+            Z.zero_offload_step(self.plan, None, self.op, self.grad_shards, self.master, self.m,
+                                self.v, self.shard16, self.flat16, self.hp, self.step_count,
+                                n_threads=self.host_threads)
         else:
             Z.zero_adamw_shard_step(self.plan, self.master, self.m, self.v, self.grad_shards,
                                     self.shard16, self.hp, self.step_count)

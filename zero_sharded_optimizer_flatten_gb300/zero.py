@@ -257,6 +257,8 @@ def _addr(t, what: str, min_numel: Optional[int] = None, dtype=None) -> int:
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{what}: expected a torch.Tensor or an int address")
+    if t.numel() == 0 and (min_numel or 0) == 0:
+        return 0  # an empty buffer is never touched (and an empty host tensor reports unpinned)
     if not t.is_cuda and not t.is_pinned():
         raise ValueError(f"{what}: tensor must be on a CUDA device or in pinned host memory")
     if not t.is_contiguous():
@@ -886,14 +888,17 @@ def zero_offload_step(plan: Plan, grads, op, grad_shards, master, m, v, out16_sh
     buffer (see zero.h): device reduce-scatter into the pinned host
     grad_shards, host AdamW + cast on the host master/m/v into the pinned
     host out16_shard, device all-gather into full_flat16 (device, or None).
+    grads None: grad_shards already hold the reduced gradients.
     chunk_elems None: the flat buffer in 8 chunks; 0: one chunk."""
     torch = _torch()
     mask = _mask(plan, rank_mask)
-    dt = _sixteen(grads) if dtype is None else dtype
+    dt = _sixteen(grads if grads is not None else out16_shard) if dtype is None else dtype
     ext = plan.flat_extent(mask)
-    if len(grads) != plan.n_ranks:
-        raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
-    g = [_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)]
+    g = None
+    if grads is not None:
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
     gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
     o16 = _per_rank(plan, out16_shard, "out16_shard", mask)
     full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
@@ -901,7 +906,7 @@ def zero_offload_step(plan: Plan, grads, op, grad_shards, master, m, v, out16_sh
         chunk_elems = max(1, -(-plan.padded // 8))
     op_i = _OPS[op] if isinstance(op, str) else int(op)
     hp = hparams.c()
-    _check(lib().zero_offload_step(plan.handle, _ptrs(g), dt, op_i, _ptrs(gs),
+    _check(lib().zero_offload_step(plan.handle, g, dt, op_i, _ptrs(gs),
                                    _host_per_rank(plan, master, "master", mask),
                                    _host_per_rank(plan, m, "m", mask),
                                    _host_per_rank(plan, v, "v", mask),
