@@ -12,9 +12,9 @@
  * Grace-Blackwell), which replaces an explicit copy; they run at the link's
  * bandwidth instead of HBM's.  Every stream argument is a cudaStream_t passed
  * as void* (NULL = the legacy default stream).  Compute calls are
- * asynchronous on that stream, except the two that run the optimizer on
- * host threads (zero_cpu_adamw_shard_step, zero_offload_step), which return
- * when the host work is done.
+ * asynchronous on that stream, except the three that run the optimizer on
+ * host threads (zero_cpu_adamw_shard_step, zero_offload_step,
+ * zero_offload_step_amp), which return when the host work is done.
  *
  * Sources (page title, section) for what each call computes:
  *  [ZeRO-2 blog]   "DeepSpeed ZeRO-2 ... DeepSpeedZeroOptimizer" (discosf.com):
@@ -502,6 +502,31 @@ zero_status zero_step_amp_reduced(const zero_plan* plan, zero_dtype dtype,
                                   const zero_amp_config* cfg, void* d_state, void* workspace,
                                   int64_t workspace_bytes, uint64_t rank_mask,
                                   int64_t bucket_elems, void* stream);
+
+/*
+ * The mixed-precision step with the optimizer offloaded to the host
+ * ([ZeRO-2 blog] §4.5 with the fp16 controls above): the device reduces
+ * (grads non-NULL, as zero_step_amp; or grads NULL, the shards and the
+ * workspace's sums of squares written by zero_reduce_scatter_bucket_amp with
+ * this bucket_elems, as zero_step_amp_reduced) and takes the decision in
+ * d_state; the host reads the decision and, unless it skips the step, host
+ * threads apply the update of zero_step_amp (gradient times the decision's
+ * coef, then AdamW with its constants) to the host master/m/v and write the
+ * host 16-bit shards, chunk by chunk, each chunk's gather into full_flat16
+ * (nullable) enqueued as soon as it is written.  Buffers, chunk_elems,
+ * n_threads, blocking and capture as zero_offload_step; d_state and
+ * workspace are device memory as for zero_step_amp.  A skipped step changes
+ * nothing on the host and launches no gather.  Results equal zero_step_amp's
+ * bit for bit.
+ */
+zero_status zero_offload_step_amp(const zero_plan* plan, const void* const* grads,
+                                  zero_dtype dtype, zero_reduce_op op, float* const* grad_shards,
+                                  float* const* master, float* const* m, float* const* v,
+                                  void* const* out16_shard, void* full_flat16,
+                                  const zero_adamw_hparams* hp, const zero_amp_config* cfg,
+                                  void* d_state, void* workspace, int64_t workspace_bytes,
+                                  uint64_t rank_mask, int64_t bucket_elems, int64_t chunk_elems,
+                                  int32_t n_threads, void* stream);
 
 /*
  * zero_step_amp without a workspace argument, for callers that cannot

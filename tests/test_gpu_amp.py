@@ -524,3 +524,94 @@ def test_reduced_path_full_size_equals_the_fused_step():
     for r in range(w.n_ranks):
         for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.gsh, b.gsh)):
             assert torch.equal(x[r].view(torch.int32), y[r].view(torch.int32)), r
+
+
+def _host_copy(seq, pin=True):
+    return [x.cpu().pin_memory() if pin else x.cpu() for x in seq]
+
+
+@pytest.mark.parametrize("numel,N,mode,dtype,bucket,chunk,reduced,threads", [
+    ((20000, 37, 4096, 3, 129), 4, "flat", "fp16", 7000, None, False, 0),
+    ((20000, 37, 4096, 3, 129), 4, "flat", "fp16", 7000, 3001, True, 3),
+    ((20000, 37, 4096, 3, 129), 4, "flat", "fp16", 0, 0, False, 2),
+    ((5000, 7, 12000, 1, 333, 9000), 3, "round_robin", "bf16", 9000, 4097, True, 5),
+])
+def test_offload_step_amp_equals_the_device_step(numel, N, mode, dtype, bucket, chunk, reduced,
+                                                 threads):
+    """The mixed-precision step with the optimizer on the host: the device
+    reduces (from the replicas, or bucket by bucket beforehand) and decides,
+    host threads update the host state and 16-bit shards, the device gathers.
+    Bit for bit like zero_step_amp on device state, and like the oracle,
+    through skipped overflows (fp16) and clipping; a skipped step changes
+    nothing on the host."""
+    w = W.small(numel, N, mode=mode, align=16, dtype=dtype, op="avg", outlier_frac=0.01)
+    cfg = Z.AmpConfig(init_scale=2.0 ** 17, min_scale=1.0, window=3, hysteresis=2,
+                      max_norm=0.05)
+    ref = AmpCase(w, cfg, bucket=bucket)
+    got = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    S = [got.plan.shard_len(r) for r in range(N)]
+    hm = _host_copy(got.master)
+    hmm, hv = _host_copy(got.m, pin=False), _host_copy(got.v, pin=False)
+    hg = [torch.zeros(n, dtype=torch.float32, pin_memory=True) for n in S]
+    h16 = [torch.zeros(n, dtype=w.torch_dtype, pin_memory=True) for n in S]
+    full = torch.zeros_like(got.full16)
+    P = got.plan.padded
+    B = bucket if bucket > 0 else P
+    skipped_seen = False
+    for t in range(1, 9):
+        g = ref.grads_scaled(t, ref.ost.scale)
+        ref.gpu_step(g)
+        ref.oracle_step_amp(g)
+        before = [x.clone() for x in hm]
+        if reduced:
+            for b in reversed(range(-(-P // B))):
+                Z.zero_reduce_scatter_bucket_amp(got.plan, g, "avg", hg, HP, got.state, got.ws, b,
+                                                 bucket_elems=bucket)
+            Z.zero_offload_step_amp(got.plan, None, "avg", hg, hm, hmm, hv, h16, full, HP, cfg,
+                                    got.state, got.ws, bucket_elems=bucket, chunk_elems=chunk,
+                                    n_threads=threads)
+        else:
+            Z.zero_offload_step_amp(got.plan, g, "avg", hg, hm, hmm, hv, h16, full, HP, cfg,
+                                    got.state, got.ws, bucket_elems=bucket, chunk_elems=chunk,
+                                    n_threads=threads)
+        torch.cuda.synchronize()
+        assert torch.equal(ref.state, got.state), t
+        if Z.read_amp_state(got.state).overflow:
+            skipped_seen = True
+            assert all(torch.equal(a, b_) for a, b_ in zip(before, hm)), t
+            continue
+        assert torch.equal(ref.full16.view(torch.int16), full.view(torch.int16)), t
+        for r in range(N):
+            for a, b_ in ((ref.master, hm), (ref.m, hmm), (ref.v, hv), (ref.gsh, hg)):
+                assert torch.equal(a[r].cpu().view(torch.int32), b_[r].view(torch.int32)), (t, r)
+            off = [int(x) for x in ref.o_seg[r][:, 2]]
+            if mode == "flat":
+                assert torch.equal(h16[r].view(torch.int16),
+                                   ref.full16[off[0]:off[0] + S[r]].cpu().view(torch.int16))
+        ref.compare_state(f"step {t}")
+        ref.compare(f"offloaded amp step {t}")
+    assert ref.ost.step >= 1
+    assert skipped_seen or dtype == "bf16"
+
+
+def test_offload_step_amp_rejects_bad_arguments_without_launching():
+    w = W.small((20000, 37), 2, mode="flat", align=16, dtype="fp16", op="avg")
+    cfg = Z.AmpConfig()
+    c = AmpCase(w, cfg, with_oracle=False)
+    S = [c.plan.shard_len(r) for r in range(2)]
+    hm = _host_copy(c.master)
+    hg = [torch.zeros(n, dtype=torch.float32, pin_memory=True) for n in S]
+    h16 = [torch.zeros(n, dtype=torch.float16, pin_memory=True) for n in S]
+    g = c.grads_scaled(1, 1.0)
+    n0 = Z.zero_launch_count()
+    with pytest.raises(Z.ZeroError, match="pinned"):
+        Z.zero_offload_step_amp(c.plan, g, "avg", [x.data_ptr() for x in c.gsh], hm, hm, hm, h16,
+                                c.full16, HP, cfg, c.state, c.ws)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Z.ZeroError, match="workspace"):
+        Z.zero_offload_step_amp(c.plan, g, "avg", hg, hm, hm, hm, h16, c.full16, HP, cfg,
+                                c.state, small)
+    with pytest.raises(Z.ZeroError, match="chunks"):
+        Z.zero_offload_step_amp(c.plan, g, "avg", hg, hm, hm, hm, h16, c.full16, HP, cfg,
+                                c.state, c.ws, chunk_elems=3)
+    assert Z.zero_launch_count() == n0

@@ -157,15 +157,18 @@ def test_engine_offload_modes_equal_the_device_engine(offload, overlap, dtype):
             assert torch.equal(xa.cpu(), xb.cpu())
 
 
-def test_engine_mixed_precision_with_host_resident_state():
-    """amp with the state in host memory: the same device decisions and
+@pytest.mark.parametrize("offload", ["host_state", "cpu"])
+def test_engine_mixed_precision_with_offload(offload):
+    """amp with the state in host memory, updated by the GPU across the link
+    or by host threads after the device's decision: the same decisions and
     updates as the device-resident engine, bit for bit (fp16, a loss scale
     that overflows at first, clipping)."""
     cfg = Z.AmpConfig(init_scale=2.0 ** 24, min_scale=1.0, window=20, hysteresis=1,
                       max_norm=1.0)
     a, b = _mlp(torch.float16), _mlp(torch.float16)
     ea = ZeroEngine(a.parameters(), 4, bucket_elems=60_000, amp=cfg)
-    eb = ZeroEngine(b.parameters(), 4, bucket_elems=60_000, amp=cfg, offload="host_state")
+    eb = ZeroEngine(b.parameters(), 4, bucket_elems=60_000, amp=cfg, offload=offload,
+                    host_threads=3)
     for t in range(1, 8):
         for q in range(4):
             x = _batch(q, t, torch.float16)
@@ -185,5 +188,3 @@ def test_engine_mixed_precision_with_host_resident_state():
 def test_engine_offload_arguments():
     with pytest.raises(ValueError):
         ZeroEngine(_mlp(torch.bfloat16).parameters(), 2, offload="nvme")
-    with pytest.raises(ValueError):
-        ZeroEngine(_mlp(torch.float16).parameters(), 2, offload="cpu", amp=Z.AmpConfig())

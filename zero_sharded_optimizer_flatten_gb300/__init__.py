@@ -12,7 +12,7 @@ from .zero import (AMP_STATE_BYTES, ZERO_BF16, ZERO_FP16, ZERO_PART_FLAT,  # noq
                    amp_state_tensor, lib, read_amp_state, zero_adamw_shard_step, zero_allgather,
                    zero_amp_init, zero_amp_workspace_bytes, zero_cpu_adamw_shard_step,
                    zero_init_shards, zero_last_error, zero_launch_count, zero_memory_bytes,
-                   zero_offload_step,
+                   zero_offload_step, zero_offload_step_amp,
                    zero_plan_describe, zero_plan_destroy, zero_plan_info, zero_plan_partitions,
                    zero_plan_segments, zero_plan_shard, zero_plan_total, zero_reduce_scatter,
                    zero_reduce_scatter_bucket_amp, zero_reduce_scatter_range,

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "zero_capi_util.h"
+#include "zero_host.h"
 #include "zero_internal.h"
 
 namespace zero {
@@ -254,7 +255,9 @@ struct HostUpdate {
   float* const* m;
   float* const* v;
   const float* const* grad_shards;
-  void* const* out16;  // nullable; entries nullable
+  void* const* out16;   // nullable; entries nullable
+  bool scaled = false;  // mixed precision: the gradient is multiplied by coef first
+  float coef = 1.0f;
 
   // Update elements [b0, b1) of the concatenation of `pieces`.
   void slice(const std::vector<HostPiece>& pieces, int64_t b0, int64_t b1) const {
@@ -265,8 +268,12 @@ struct HostUpdate {
       if (lo < hi) {
         const int64_t o = pc.off + (lo - seen);
         uint16_t* o16 = out16 && out16[pc.r] ? static_cast<uint16_t*>(out16[pc.r]) + o : nullptr;
-        cpu_adamw_range(sc, dtype, master[pc.r] + o, m[pc.r] + o, v[pc.r] + o,
-                        grad_shards[pc.r] + o, o16, hi - lo);
+        if (scaled)
+          cpu_adamw_range_scaled(sc, coef, dtype, master[pc.r] + o, m[pc.r] + o, v[pc.r] + o,
+                                 grad_shards[pc.r] + o, o16, hi - lo);
+        else
+          cpu_adamw_range(sc, dtype, master[pc.r] + o, m[pc.r] + o, v[pc.r] + o,
+                          grad_shards[pc.r] + o, o16, hi - lo);
       }
       seen += pc.len;
     }
@@ -591,14 +598,14 @@ enum class AmpStats {
 };
 
 // The mixed-precision step: the sums of squares as `stats` says, then the
-// decision kernel and the update (k_adamw_amp).
+// decision kernel and, unless `decide_only`, the update (k_adamw_amp).
 zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* grads,
                      AmpStats stats_from, zero_dtype dtype, zero_reduce_op op,
                      float* const* grad_shards, float* const* master, float* const* m,
                      float* const* v, void* full_flat16, void* const* out16_shard,
                      const zero_adamw_hparams* hp, const zero_amp_config* cfg, void* d_state,
                      void* workspace, int64_t workspace_bytes, uint64_t rank_mask,
-                     int64_t bucket_elems, void* stream) {
+                     int64_t bucket_elems, void* stream, bool decide_only = false) {
   ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
   ZERO_TRY(check_dtype(fn, dtype));
   if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
@@ -673,6 +680,7 @@ zero_status amp_step(const char* fn, const zero_plan* plan, const void* const* g
     return fail(ZERO_ERR_CUDA, "%s: launch failed: %s", fn,
                 cudaGetErrorString(static_cast<cudaError_t>(err)));
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (decide_only) return ZERO_OK;
   return run_buckets(fn, Kind::kAdamwAmp, dtype, plan, rank_mask, 0, a, stream);
 }
 
@@ -924,6 +932,42 @@ zero_status check_host_buffers(const char* fn, const char* what, void* const* ar
   return ZERO_OK;
 }
 
+// The checks both offload steps make after the plain argument checks: the
+// stream is not capturing (the host waits for the device), the buffers are
+// where the host and the device can reach them, and the chunking is bounded.
+zero_status check_offload(const char* fn, const zero_plan* plan, uint64_t mask,
+                          float* const* grad_shards, float* const* master, float* const* m,
+                          float* const* v, void* const* out16_shard, void* full_flat16,
+                          int64_t chunk_elems, void* stream, int64_t* C, int64_t* K) {
+  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, mask, false));
+  ZERO_TRY(check_ptrs(fn, "master", master, plan, mask, false));
+  ZERO_TRY(check_ptrs(fn, "m", m, plan, mask, false));
+  ZERO_TRY(check_ptrs(fn, "v", v, plan, mask, false));
+  ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, mask, false));
+  if (full_flat16 && !aligned16(full_flat16))
+    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+  const int64_t total = plan->padded;
+  *C = chunk_elems > 0 ? chunk_elems : std::max<int64_t>(total, 1);
+  *K = (total + *C - 1) / *C;
+  if (*K > kMaxOffloadChunks)
+    return fail(ZERO_ERR_INVALID, "%s: %" PRId64 " chunks of %" PRId64 " elements; at most %d",
+                fn, *K, *C, kMaxOffloadChunks);
+  ZERO_TRY(pending_error(fn));
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  ZERO_TRY(cuda_ok(fn, "cudaStreamIsCapturing",
+                   cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap)));
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(ZERO_ERR_UNSUPPORTED, "%s: cannot be captured: the host waits for the device", fn);
+  ZERO_TRY(check_host_buffers(fn, "grad_shards", reinterpret_cast<void* const*>(grad_shards),
+                              plan, mask, true));
+  ZERO_TRY(check_host_buffers(fn, "out16_shard", out16_shard, plan, mask, true));
+  ZERO_TRY(check_host_buffers(fn, "master", reinterpret_cast<void* const*>(master), plan, mask,
+                              false));
+  ZERO_TRY(check_host_buffers(fn, "m", reinterpret_cast<void* const*>(m), plan, mask, false));
+  ZERO_TRY(check_host_buffers(fn, "v", reinterpret_cast<void* const*>(v), plan, mask, false));
+  return ZERO_OK;
+}
+
 // Launch `kind` over the masked ranks' elements of the flat range [lo, hi),
 // ordered after everything before it on the stream.
 zero_status launch_range(const char* fn, Kind kind, zero_dtype dtype, const zero_plan* plan,
@@ -946,62 +990,29 @@ struct OffloadSync {
   std::vector<int> done;
 };
 
-}  // namespace
-
-extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* const* grads,
-                                         zero_dtype dtype, zero_reduce_op op,
-                                         float* const* grad_shards, float* const* master,
-                                         float* const* m, float* const* v,
-                                         void* const* out16_shard, void* full_flat16,
-                                         const zero_adamw_hparams* hp, int64_t step,
-                                         uint64_t rank_mask, int64_t chunk_elems,
-                                         int32_t n_threads, void* stream) {
-  const char* fn = "zero_offload_step";
-  NvtxRange nvtx_range(fn);
-  clear_error();
-  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
-  ZERO_TRY(check_dtype(fn, dtype));
-  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
-  ZERO_TRY(check_hparams(fn, hp, step));
-  if (grads) ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
-  ZERO_TRY(check_ptrs(fn, "grad_shards", grad_shards, plan, rank_mask, false));
-  ZERO_TRY(check_ptrs(fn, "master", master, plan, rank_mask, false));
-  ZERO_TRY(check_ptrs(fn, "m", m, plan, rank_mask, false));
-  ZERO_TRY(check_ptrs(fn, "v", v, plan, rank_mask, false));
-  ZERO_TRY(check_ptrs(fn, "out16_shard", out16_shard, plan, rank_mask, false));
-  if (full_flat16 && !aligned16(full_flat16))
-    return fail(ZERO_ERR_ALIGN, "%s: full_flat16 is not 16-byte aligned", fn);
+// The host update of every chunk of C flat elements (K chunks) by n_threads
+// workers, each chunk's gather into full_flat16 (nullable) enqueued on
+// `stream` as soon as the workers have written it.  Chunk k is released to
+// the workers when event ev[k] has completed (n_events == K), all chunks when
+// ev[0] has (n_events == 1), or at once (n_events == 0).
+zero_status host_update_pipeline(const char* fn, const zero_plan* plan, uint64_t mask,
+                                 zero_dtype dtype, const HostUpdate& up, int64_t C, int64_t K,
+                                 const std::vector<cudaEvent_t>* ev, int64_t n_events,
+                                 void* const* out16_shard, void* full_flat16,
+                                 int32_t n_threads, void* stream) {
   const int64_t total = plan->padded;
-  const int64_t C = chunk_elems > 0 ? chunk_elems : std::max<int64_t>(total, 1);
-  const int64_t K = (total + C - 1) / C;
-  if (K > kMaxOffloadChunks)
-    return fail(ZERO_ERR_INVALID, "%s: %" PRId64 " chunks of %" PRId64 " elements; at most %d",
-                fn, K, C, kMaxOffloadChunks);
-  ZERO_TRY(pending_error(fn));
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  ZERO_TRY(cuda_ok(fn, "cudaStreamIsCapturing",
-                   cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap)));
-  if (cap != cudaStreamCaptureStatusNone)
-    return fail(ZERO_ERR_UNSUPPORTED, "%s: cannot be captured: the host waits for the device", fn);
-  ZERO_TRY(check_host_buffers(fn, "grad_shards", reinterpret_cast<void* const*>(grad_shards),
-                              plan, rank_mask, true));
-  ZERO_TRY(check_host_buffers(fn, "out16_shard", out16_shard, plan, rank_mask, true));
-  ZERO_TRY(check_host_buffers(fn, "master", reinterpret_cast<void* const*>(master), plan,
-                              rank_mask, false));
-  ZERO_TRY(check_host_buffers(fn, "m", reinterpret_cast<void* const*>(m), plan, rank_mask, false));
-  ZERO_TRY(check_host_buffers(fn, "v", reinterpret_cast<void* const*>(v), plan, rank_mask, false));
-  if (K == 0) return ZERO_OK;
-
   // each chunk's host pieces: the masked ranks' runs cut to the chunk
   std::vector<std::vector<HostPiece>> pieces;
   std::vector<int64_t> chunk_len;
+  OffloadSync sync;
   try {
     pieces.resize(static_cast<size_t>(K));
     chunk_len.assign(static_cast<size_t>(K), 0);
+    sync.done.assign(static_cast<size_t>(K), 0);
     for (int64_t k = 0; k < K; ++k) {
       const int64_t lo = k * C, hi = std::min(total, lo + C);
       for (int r = 0; r < plan->n_ranks; ++r) {
-        if (!in_mask(rank_mask, r)) continue;
+        if (!in_mask(mask, r)) continue;
         for (const auto& run : plan->runs[r]) {
           const int64_t a = std::max(lo, run.flat_off);
           const int64_t b = std::min(hi, run.flat_off + run.len);
@@ -1014,50 +1025,19 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   } catch (const std::bad_alloc&) {
     return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
   }
-
-  ArgsHolder red(new_args()), gat(new_args());
-  if (!red.p || !gat.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
-  for (int r = 0; r < plan->n_ranks; ++r) {
-    red.p->grads[r] = grads ? grads[r] : nullptr;
-    if (!in_mask(rank_mask, r)) continue;
-    red.p->gshard[r] = grad_shards[r];
-    gat.p->shard16[r] = out16_shard[r];
-  }
-  set_scale(*red.p, plan->n_ranks, op);
-  set_bounds(*red.p, plan);
+  ArgsHolder gat(new_args());
+  if (!gat.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  for (int r = 0; r < plan->n_ranks; ++r)
+    if (in_mask(mask, r)) gat.p->shard16[r] = out16_shard[r];
   gat.p->full16 = full_flat16;
   set_bounds(*gat.p, plan);
+  if (n_events == 0) sync.ready = K;
 
-  // 1. every chunk's reduction, each followed by its event; without grads
-  //    (the shards already hold the reduced gradients) one event marks the
-  //    end of the work enqueued on the stream before the call
-  std::vector<cudaEvent_t>* ev = nullptr;
-  const int64_t n_events = grads ? K : 1;
-  ZERO_TRY(pool_events(fn, static_cast<size_t>(n_events), &ev, true));
-  for (int64_t k = 0; k < n_events; ++k) {
-    if (grads) {
-      const int64_t lo = k * C, hi = std::min(total, lo + C);
-      ZERO_TRY(launch_range(fn, Kind::kReduceScatter, dtype, plan, rank_mask, lo, hi, *red.p,
-                            stream));
-    }
-    ZERO_TRY(cuda_ok(fn, "cudaEventRecord",
-                     cudaEventRecord((*ev)[k], static_cast<cudaStream_t>(stream))));
-  }
-
-  // 2. host workers: worker j updates the j-th of nt equal slices of each
-  //    chunk as soon as that chunk's reduction has completed
-  const HostUpdate up{make_scalars(*hp, step), dtype, master, m, v, grad_shards, out16_shard};
   // the calling thread waits for the device and launches the gathers, so by
   // default one hardware thread is left to it
   int nt = n_threads > 0 ? n_threads
                          : static_cast<int>(std::thread::hardware_concurrency()) - 1;
   nt = std::max(1, std::min(nt, kMaxHostThreads));
-  OffloadSync sync;
-  try {
-    sync.done.assign(static_cast<size_t>(K), 0);
-  } catch (const std::bad_alloc&) {
-    return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
-  }
   auto worker = [&](int j) {
     for (int64_t k = 0; k < K; ++k) {
       {
@@ -1087,8 +1067,8 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
     return stop(fail(ZERO_ERR_OOM, "%s: could not start host threads", fn));
   }
 
-  // 3. release each chunk to the workers when its reduction is done; gather
-  //    every chunk the workers have finished, as soon as it is finished
+  // release the chunks as their events complete; gather every chunk the
+  // workers have finished, as soon as it is finished
   int64_t gathered = 0;
   auto gather_finished = [&](bool wait_all) -> zero_status {
     while (gathered < K) {
@@ -1101,8 +1081,8 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
       }
       const int64_t lo = gathered * C, hi = std::min(total, lo + C);
       if (full_flat16) {
-        const zero_status st = launch_range(fn, Kind::kAllgather, dtype, plan, rank_mask, lo,
-                                            hi, *gat.p, stream);
+        const zero_status st = launch_range(fn, Kind::kAllgather, dtype, plan, mask, lo, hi,
+                                            *gat.p, stream);
         if (st != ZERO_OK) return st;
       }
       ++gathered;
@@ -1112,11 +1092,11 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   for (int64_t k = 0; k < n_events; ++k) {
     const cudaError_t e = cudaEventSynchronize((*ev)[k]);
     if (e != cudaSuccess)
-      return stop(fail(ZERO_ERR_CUDA, "%s: reduction of chunk %" PRId64 ": %s", fn, k,
+      return stop(fail(ZERO_ERR_CUDA, "%s: device work before chunk %" PRId64 ": %s", fn, k,
                        cudaGetErrorString(e)));
     {
       std::lock_guard<std::mutex> lk(sync.mu);
-      sync.ready = grads ? k + 1 : K;
+      sync.ready = n_events == K ? k + 1 : K;
     }
     sync.ready_cv.notify_all();
     const zero_status st = gather_finished(false);
@@ -1126,6 +1106,97 @@ extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* cons
   if (st != ZERO_OK) return stop(st);
   for (auto& th : threads) th.join();
   return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" zero_status zero_offload_step(const zero_plan* plan, const void* const* grads,
+                                         zero_dtype dtype, zero_reduce_op op,
+                                         float* const* grad_shards, float* const* master,
+                                         float* const* m, float* const* v,
+                                         void* const* out16_shard, void* full_flat16,
+                                         const zero_adamw_hparams* hp, int64_t step,
+                                         uint64_t rank_mask, int64_t chunk_elems,
+                                         int32_t n_threads, void* stream) {
+  const char* fn = "zero_offload_step";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  ZERO_TRY(check_dtype(fn, dtype));
+  if (op != ZERO_REDUCE_SUM && op != ZERO_REDUCE_AVG) return fail(ZERO_ERR_INVALID, "%s: unknown reduce op", fn);
+  ZERO_TRY(check_hparams(fn, hp, step));
+  if (grads) ZERO_TRY(check_ptrs(fn, "grads", grads, plan, rank_mask, false, true));
+  int64_t C = 0, K = 0;
+  ZERO_TRY(check_offload(fn, plan, rank_mask, grad_shards, master, m, v, out16_shard,
+                         full_flat16, chunk_elems, stream, &C, &K));
+  if (K == 0) return ZERO_OK;
+  const int64_t total = plan->padded;
+
+  // every chunk's reduction, each followed by its event; without grads (the
+  // shards already hold the reduced gradients) one event marks the end of
+  // the work enqueued on the stream before the call
+  ArgsHolder red(new_args());
+  if (!red.p) return fail(ZERO_ERR_OOM, "%s: out of host memory", fn);
+  for (int r = 0; r < plan->n_ranks; ++r) {
+    red.p->grads[r] = grads ? grads[r] : nullptr;
+    if (in_mask(rank_mask, r)) red.p->gshard[r] = grad_shards[r];
+  }
+  set_scale(*red.p, plan->n_ranks, op);
+  set_bounds(*red.p, plan);
+  std::vector<cudaEvent_t>* ev = nullptr;
+  const int64_t n_events = grads ? K : 1;
+  ZERO_TRY(pool_events(fn, static_cast<size_t>(n_events), &ev, true));
+  for (int64_t k = 0; k < n_events; ++k) {
+    if (grads) {
+      const int64_t lo = k * C, hi = std::min(total, lo + C);
+      ZERO_TRY(launch_range(fn, Kind::kReduceScatter, dtype, plan, rank_mask, lo, hi, *red.p,
+                            stream));
+    }
+    ZERO_TRY(cuda_ok(fn, "cudaEventRecord",
+                     cudaEventRecord((*ev)[k], static_cast<cudaStream_t>(stream))));
+  }
+  const HostUpdate up{make_scalars(*hp, step), dtype, master, m, v, grad_shards, out16_shard};
+  return host_update_pipeline(fn, plan, rank_mask, dtype, up, C, K, ev, n_events, out16_shard,
+                              full_flat16, n_threads, stream);
+}
+
+extern "C" zero_status zero_offload_step_amp(
+    const zero_plan* plan, const void* const* grads, zero_dtype dtype, zero_reduce_op op,
+    float* const* grad_shards, float* const* master, float* const* m, float* const* v,
+    void* const* out16_shard, void* full_flat16, const zero_adamw_hparams* hp,
+    const zero_amp_config* cfg, void* d_state, void* workspace, int64_t workspace_bytes,
+    uint64_t rank_mask, int64_t bucket_elems, int64_t chunk_elems, int32_t n_threads,
+    void* stream) {
+  const char* fn = "zero_offload_step_amp";
+  NvtxRange nvtx_range(fn);
+  clear_error();
+  ZERO_TRY(check_plan_mask(fn, plan, rank_mask));
+  int64_t C = 0, K = 0;
+  ZERO_TRY(check_offload(fn, plan, rank_mask, grad_shards, master, m, v, out16_shard,
+                         full_flat16, chunk_elems, stream, &C, &K));
+  // the sums of squares (from the replicas, or already in the workspace) and
+  // the decision kernel; amp_step checks its own arguments before launching
+  ZERO_TRY(amp_step(fn, plan, grads, grads ? AmpStats::kReplicas : AmpStats::kDone, dtype, op,
+                    grad_shards, master, m, v, full_flat16, out16_shard, hp, cfg, d_state,
+                    workspace, workspace_bytes, rank_mask, bucket_elems, stream, true));
+  // the host reads the decision
+  zero_amp_state st;
+  std::vector<cudaEvent_t>* ev = nullptr;
+  ZERO_TRY(pool_events(fn, 1, &ev, true));
+  ZERO_TRY(cuda_ok(fn, "cudaMemcpyAsync",
+                   cudaMemcpyAsync(&st, d_state, sizeof st, cudaMemcpyDeviceToHost,
+                                   static_cast<cudaStream_t>(stream))));
+  ZERO_TRY(cuda_ok(fn, "cudaEventRecord",
+                   cudaEventRecord((*ev)[0], static_cast<cudaStream_t>(stream))));
+  ZERO_TRY(cuda_ok(fn, "cudaEventSynchronize", cudaEventSynchronize((*ev)[0])));
+  if (st.overflow != 0 || K == 0) return ZERO_OK;  // skipped: nothing changes
+  HostUpdate up{StepScalars{}, dtype, master, m, v, grad_shards, out16_shard};
+  up.sc = StepScalars{st.sc[0], st.sc[1], st.sc[2], st.sc[3], st.sc[4], st.sc[5], st.sc[6],
+                      st.sc[7]};
+  up.scaled = true;
+  up.coef = st.coef;
+  return host_update_pipeline(fn, plan, rank_mask, dtype, up, C, K, nullptr, 0, out16_shard,
+                              full_flat16, n_threads, stream);
 }
 
 extern "C" zero_status zero_sync(void* stream) {

@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "zero_host.h"
 #include "zero_internal.h"
 
 namespace zero {
@@ -35,12 +36,14 @@ inline uint16_t to_fp16(float x) {
 
 enum Cast { kNoCast, kCastBf16, kCastFp16 };
 
-template <Cast C>
-void adamw_loop(const StepScalars& s, float* __restrict p, float* __restrict m,
+// kScaled: the gradient is multiplied by `coef` first (one rounding), as the
+// mixed-precision update does.
+template <Cast C, bool kScaled>
+void adamw_loop(const StepScalars& s, float coef, float* __restrict p, float* __restrict m,
                 float* __restrict v, const float* __restrict g, uint16_t* __restrict out16,
                 int64_t n) {
   for (int64_t i = 0; i < n; ++i) {
-    const float gi = g[i];
+    const float gi = kScaled ? g[i] * coef : g[i];
     float pp = p[i] * s.d;
     const float mm = s.b1 * m[i] + s.c1 * gi;
     const float vv = s.b2 * v[i] + s.c2 * (gi * gi);
@@ -56,14 +59,29 @@ void adamw_loop(const StepScalars& s, float* __restrict p, float* __restrict m,
 
 }  // namespace
 
+namespace {
+
+template <bool kScaled>
+void adamw_dispatch(const StepScalars& s, float coef, zero_dtype dtype, float* p, float* m,
+                    float* v, const float* g, uint16_t* out16, int64_t n) {
+  if (!out16)
+    adamw_loop<kNoCast, kScaled>(s, coef, p, m, v, g, nullptr, n);
+  else if (dtype == ZERO_BF16)
+    adamw_loop<kCastBf16, kScaled>(s, coef, p, m, v, g, out16, n);
+  else
+    adamw_loop<kCastFp16, kScaled>(s, coef, p, m, v, g, out16, n);
+}
+
+}  // namespace
+
 void cpu_adamw_range(const StepScalars& s, zero_dtype dtype, float* p, float* m, float* v,
                      const float* g, uint16_t* out16, int64_t n) {
-  if (!out16)
-    adamw_loop<kNoCast>(s, p, m, v, g, nullptr, n);
-  else if (dtype == ZERO_BF16)
-    adamw_loop<kCastBf16>(s, p, m, v, g, out16, n);
-  else
-    adamw_loop<kCastFp16>(s, p, m, v, g, out16, n);
+  adamw_dispatch<false>(s, 1.0f, dtype, p, m, v, g, out16, n);
+}
+
+void cpu_adamw_range_scaled(const StepScalars& s, float coef, zero_dtype dtype, float* p,
+                            float* m, float* v, const float* g, uint16_t* out16, int64_t n) {
+  adamw_dispatch<true>(s, coef, dtype, p, m, v, g, out16, n);
 }
 
 }  // namespace zero

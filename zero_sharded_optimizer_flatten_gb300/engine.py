@@ -34,11 +34,12 @@ asks ("DeepSpeed ZeRO-2 ..." §4.5).  ``offload="cpu"`` is that form: the
 bucket reductions write the fp32 gradient shards into pinned host memory
 across the host link, ``step()`` runs AdamW + cast on host threads and
 all-gathers the host 16-bit shards, chunk by chunk so that the gathers
-overlap the update (``zero_offload_step`` on the reduced shards).
-``offload="host_state"`` keeps the update on the GPU, whose kernels read and
-write the host-resident master/m/v across NVLink-C2C (no host
-synchronisation; works with ``amp`` too).  Both give the device engine's
-results bit for bit.
+overlap the update (``zero_offload_step`` on the reduced shards; with ``amp`` the device
+still takes the decision and the host applies it,
+``zero_offload_step_amp``).  ``offload="host_state"`` keeps the update on
+the GPU, whose kernels read and write the host-resident master/m/v across
+NVLink-C2C (no host synchronisation).  Both give the device engine's results
+bit for bit.
 
 The arithmetic is the library's (no compute happens here); this module only
 does bookkeeping and launches.
@@ -70,9 +71,6 @@ class ZeroEngine:
                 raise ValueError("all parameters must share one 16-bit dtype and one CUDA device")
         if offload not in (None, "cpu", "host_state"):
             raise ValueError("offload must be None, 'cpu' or 'host_state'")
-        if offload == "cpu" and amp is not None:
-            raise ValueError("the CPU optimizer has no mixed-precision controls; use "
-                             "offload='host_state' with amp")
         self.offload, self.host_threads = offload, host_threads
         self.n_ranks, self.op = n_ranks, op
         self.hp = hparams or Z.AdamW()
@@ -212,7 +210,15 @@ class ZeroEngine:
         if self.reduction_stream is not None:
             torch.cuda.current_stream().wait_stream(self.reduction_stream)
         self.step_count += 1
-        if self.amp is not None:
+        if self.amp is not None and self.offload == "cpu":
+            # the device decides (skip, loss scale, clipping); the host reads
+            # the decision and updates; the gathers overlap the update
+            Z.zero_offload_step_amp(self.plan, None, self.op, self.grad_shards, self.master,
+                                    self.m, self.v, self.shard16, self.flat16, self.hp, self.amp,
+                                    self.amp_state, self._workspace,
+                                    bucket_elems=self.bucket_elems,
+                                    n_threads=self.host_threads)
+        elif self.amp is not None:
             # the step count that AdamW uses lives in the device state (skipped
             # steps do not count)
             Z.zero_step_amp_reduced(self.plan, self.grad_shards, self.master, self.m, self.v,

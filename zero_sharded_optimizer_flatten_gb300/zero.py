@@ -96,6 +96,9 @@ def lib():
                                               u64, i32],
                 "zero_offload_step": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp,
                                       vpp, vp, hp, i64, u64, i64, i32, vp],
+                "zero_offload_step_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp,
+                                          vpp, vpp, vp, hp, ctypes.POINTER(AmpConfigC), vp, vp,
+                                          i64, u64, i64, i64, i32, vp],
                 "zero_amp_init": [vp, ctypes.POINTER(AmpConfigC), vp],
                 "zero_amp_workspace_bytes": [vp, u64, i64, i64p],
                 "zero_step_amp": [vp, vpp, ctypes.c_int, ctypes.c_int, vpp, vpp, vpp, vpp, vp,
@@ -913,6 +916,43 @@ def zero_offload_step(plan: Plan, grads, op, grad_shards, master, m, v, out16_sh
                                    _ptrs(o16), full, ctypes.byref(hp), int(step), mask,
                                    int(chunk_elems), int(n_threads), _stream(stream)))
 
+
+def zero_offload_step_amp(plan: Plan, grads, op, grad_shards, master, m, v, out16_shard,
+                          full_flat16, hparams: AdamW, cfg: AmpConfig, state, workspace,
+                          rank_mask=None, bucket_elems=0, chunk_elems: Optional[int] = None,
+                          n_threads: int = 0, stream=None, dtype=None):
+    """The mixed-precision step with the optimizer on the host (see zero.h):
+    device reduction and decision, host AdamW + cast of the host state into
+    the pinned host out16_shard, device gather of each finished chunk.
+    grads None: grad_shards and the workspace's sums of squares were written
+    by zero_reduce_scatter_bucket_amp with the same bucket_elems."""
+    torch = _torch()
+    mask = _mask(plan, rank_mask)
+    dt = _sixteen(grads if grads is not None else out16_shard) if dtype is None else dtype
+    ext = plan.flat_extent(mask)
+    g = None
+    if grads is not None:
+        if len(grads) != plan.n_ranks:
+            raise ValueError(f"grads: expected {plan.n_ranks} replicas, got {len(grads)}")
+        g = _ptrs([_addr(t, f"grads[{q}]", ext) for q, t in enumerate(grads)])
+    gs = _per_rank(plan, grad_shards, "grad_shards", mask, torch.float32)
+    o16 = _per_rank(plan, out16_shard, "out16_shard", mask)
+    full = _addr(full_flat16, "full_flat16", ext) if full_flat16 is not None else None
+    if chunk_elems is None:
+        chunk_elems = max(1, -(-plan.padded // 8))
+    op_i = _OPS[op] if isinstance(op, str) else int(op)
+    hp, c = hparams.c(), cfg.c()
+    ws_bytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) \
+        else zero_amp_workspace_bytes(plan, mask, bucket_elems)
+    _check(lib().zero_offload_step_amp(plan.handle, g, dt, op_i, _ptrs(gs),
+                                       _host_per_rank(plan, master, "master", mask),
+                                       _host_per_rank(plan, m, "m", mask),
+                                       _host_per_rank(plan, v, "v", mask),
+                                       _ptrs(o16), full, ctypes.byref(hp), ctypes.byref(c),
+                                       _addr(state, "d_state", AMP_STATE_BYTES),
+                                       _addr(workspace, "workspace"), ws_bytes, mask,
+                                       int(bucket_elems), int(chunk_elems), int(n_threads),
+                                       _stream(stream)))
 
 # ----------------------------------------------------------------------------
 # the plan queries under their C names (the Plan object caches the same data)
