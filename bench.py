@@ -409,6 +409,8 @@ class FlatRunner:
                       for s in range(grad_sets)]
         self.elems = sum(S)                       # work units per step
         self.padded = plan.padded
+        # offload: the kernels read and write master/m/v across the host link
+        self.link_bytes_per_step = 24 * self.elems if offload else 0
         if amp is None:
             self.calls = [Z.ZeroStep(plan, g, w.op, self.master, self.m, self.v, self.full16,
                                      None, self.hp, rank_mask=self.mask,
@@ -574,12 +576,16 @@ class Zero3Runner:
     shard (the next gather's source).  One gradient set is shared by all
     layers (the backward pass refills one buffer per layer)."""
 
-    def __init__(self, w, dev, layer_states, prefetch=0):
+    def __init__(self, w, dev, layer_states, prefetch=0, offload=False):
         import torch
 
         import zero_sharded_optimizer_flatten_gb300 as Z
         from zero_sharded_optimizer_flatten_gb300 import workloads as W
         self.Z, self.w, self.dev = Z, w, dev
+        # offload: every layer's 16-bit shards and fp32 master/m/v live in
+        # pinned host memory; the gathers and steps stream them across the
+        # host link (the replicas and the layer buffers stay in HBM)
+        self.offload = offload
         self.plan = plan = Z.zero_plan_partitions(list(w.numel), w.n_ranks, w.mode, w.align)
         self.hp = Z.AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01)
         L = plan.padded
@@ -588,12 +594,18 @@ class Zero3Runner:
         self.grads = [W.grads16(w, 1, q, dev, 0, L) for q in range(w.n_ranks)]
         self.n_states = min(w.layers, layer_states)
         self.shards, self.calls, self.states = [], [], []
+        def state(n, dtype):
+            if offload:
+                return torch.empty(n, dtype=dtype, pin_memory=True)
+            return torch.empty(n, dtype=dtype, device=dev)
         for layer in range(self.n_states):
             p16 = W.params16(w, dev, L, layer=layer)
-            sh = [p16[sum(S[:r]):sum(S[:r]) + S[r]].clone() for r in range(w.n_ranks)]
-            master = [torch.empty(n, dtype=torch.float32, device=dev) for n in S]
-            m = [torch.empty_like(x) for x in master]
-            v = [torch.empty_like(x) for x in master]
+            sh = [state(S[r], w.torch_dtype) for r in range(w.n_ranks)]
+            for r in range(w.n_ranks):
+                sh[r].copy_(p16[sum(S[:r]):sum(S[:r]) + S[r]])
+            master = [state(n, torch.float32) for n in S]
+            m = [state(n, torch.float32) for n in S]
+            v = [state(n, torch.float32) for n in S]
             Z.zero_init_shards(plan, p16, master, m, v)
             del p16
             self.shards.append(sh)
@@ -615,6 +627,9 @@ class Zero3Runner:
         self.bytes_per_step = w.layers * (step_bytes(plan.padded, w.n_ranks) + 4 * plan.padded)
         self.kernel_bytes = step_bytes(plan.padded, w.n_ranks)  # per k_step launch
         self.kernel = KERNEL_PREFIX
+        # across the host link per element and layer: the gather reads the
+        # 16-bit shard, the step reads and writes master/m/v and writes it
+        self.link_bytes_per_step = 28 * self.elems if offload else 0
 
     def step(self, t, events=None):
         if self.prefetch:
@@ -663,7 +678,7 @@ PER_CONFIG = (
 def make_runner(w, dev, grad_sets=2, amp=None, offload=False, from_shards=False,
                 layer_states=40, prefetch=0, reduced=False):
     if w.zero3:
-        return Zero3Runner(w, dev, layer_states, prefetch)
+        return Zero3Runner(w, dev, layer_states, prefetch, offload)
     return FlatRunner(w, dev, grad_sets, amp, offload, from_shards, reduced)
 
 
@@ -1010,9 +1025,11 @@ def run_gpu(args, world, rank, local):
             "launches_per_step": nb,
             "achieved_from": "bytes of the step's launches / their back-to-back time"})
     if args.offload:
-        link = 24 * run.elems
+        link = run.link_bytes_per_step
         line["config"]["offload"] = {
-            "state": "fp32 master/m/v in pinned host memory, streamed by the kernels",
+            "state": ("every layer's 16-bit shards and fp32 master/m/v in pinned host memory, "
+                      "streamed by the gathers and steps" if w.zero3 else
+                      "fp32 master/m/v in pinned host memory, streamed by the kernels"),
             "host_link_bytes_per_step": link,
             "hbm_bytes_per_step": run.bytes_per_step - link,
         }

@@ -153,3 +153,38 @@ def test_zero3_pass_rejects_a_bad_layer_before_launching():
         passer(1)
     assert e.value.status == Z.ZERO_ERR_ALIGN and "layer 2" in str(e.value)
     assert Z.zero_launch_count() == before
+
+
+@pytest.mark.parametrize("two_streams", [False, True])
+def test_zero3_pass_with_layer_state_in_host_memory(two_streams):
+    """ZeRO-3 with the layers' state offloaded: every layer's 16-bit shards
+    and fp32 master/m/v live in pinned host memory (the gradient replicas and
+    the layer buffers stay in HBM); the gathers read the shards and the steps
+    update the state across the host link.  Bit for bit the device-resident
+    pass."""
+    cfg = ZERO3_LAYOUTS["flat_bf16_N4"]
+    N = cfg["N"]
+    w = W.small(cfg["numel"], N, mode=cfg["mode"], align=cfg["align"], dtype=cfg["dtype"],
+                op=cfg["op"])
+    plan = Z.zero_plan_partitions(list(w.numel), N, w.mode, w.align)
+    n_layers = 4
+    dev = _layers(w, plan, n_layers)
+    host = _layers(w, plan, n_layers)
+    for L in host:
+        for key in ("shards16", "master", "m", "v"):
+            L[key] = [x.cpu().pin_memory() for x in L[key]]
+    dbufs = [torch.zeros(plan.padded, dtype=w.torch_dtype, device="cuda") for _ in range(2)]
+    hbufs = [torch.zeros(plan.padded, dtype=w.torch_dtype, device="cuda") for _ in range(2)]
+    gather = torch.cuda.Stream() if two_streams else None
+    pass_dev = Z.Zero3Pass(plan, dev, dbufs, w.op, HP)
+    pass_host = Z.Zero3Pass(plan, host, hbufs, w.op, HP)
+    for t in (1, 2, 3):
+        pass_dev(t, gather_stream=gather)
+        pass_host(t, gather_stream=gather)
+    torch.cuda.synchronize()
+    for layer in range(n_layers):
+        for r in range(N):
+            for key in ("master", "m", "v", "shards16"):
+                assert torch.equal(host[layer][key][r], dev[layer][key][r].cpu()), (layer, key)
+    for b in range(2):
+        assert torch.equal(hbufs[b], dbufs[b])
