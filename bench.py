@@ -1116,9 +1116,24 @@ def run_offload_cpu(args, world, rank, local):
             acc["cpu_adamw"] += t2 - t1
             acc["gather"] += t3 - t2
 
+    amp = None
+    if args.amp:
+        # the mixed-precision form: the device reduces, sums the squares and
+        # decides; the host applies the decision (scale 1, clipping active)
+        amp = Z.AmpConfig(init_scale=1.0, min_scale=1.0, window=1000, hysteresis=2,
+                          max_norm=args.max_norm)
+        state = Z.amp_state_tensor(dev)
+        Z.zero_amp_init(state, amp)
+        ws = torch.empty(max(16, Z.zero_amp_workspace_bytes(plan)), dtype=torch.uint8,
+                         device=dev)
+
     def pipelined(t, acc=None):
-        Z.zero_offload_step(plan, grads, w.op, gsh, master, m, v, s16, full16, hp, t,
-                            chunk_elems=chunk, n_threads=args.threads)
+        if amp is not None:
+            Z.zero_offload_step_amp(plan, grads, w.op, gsh, master, m, v, s16, full16, hp, amp,
+                                    state, ws, chunk_elems=chunk, n_threads=args.threads)
+        else:
+            Z.zero_offload_step(plan, grads, w.op, gsh, master, m, v, s16, full16, hp, t,
+                                chunk_elems=chunk, n_threads=args.threads)
         Z.zero_sync()
 
     t = 0
@@ -1146,7 +1161,9 @@ def run_offload_cpu(args, world, rank, local):
                        "offload": "CPU optimizer: fp32 state in pinned host memory, AdamW + cast "
                                   "on host threads, GPU reduce-scatter and all-gather across the "
                                   f"host link, overlapped in chunks of {chunk} flat elements "
-                                  "(zero_offload_step)",
+                                  + ("(zero_offload_step_amp: mixed-precision controls decided on "
+                                     "the device, clipping active)" if amp is not None
+                                     else "(zero_offload_step)"),
                        "host_threads": threads,
                        "serial": {"ms_per_step": 1e3 * el_serial / args.steps,
                                   "ms_per_phase": {k: 1e3 * x / args.steps
