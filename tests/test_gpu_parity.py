@@ -191,6 +191,67 @@ def test_non_default_stream():
     assert c is not None
 
 
+def test_calls_from_several_host_threads():
+    """The library keeps no shared mutable state between calls (plans are
+    read-only; launch arguments are per call, events per thread, the error
+    message thread-local): four host threads, each stepping its own group on
+    its own stream (bucketed fused steps or the three unfused calls) and then
+    failing one call on purpose, give the results of the same calls made one
+    thread at a time, and each thread reads its own error message."""
+    import threading
+    w = W.small((30000, 37, 4096, 3, 129), 4, mode="flat", align=16, dtype="bf16", op="avg")
+
+    def make():
+        c = Case(w, with_oracle=False)
+        c.gsh = [torch.empty(c.plan.shard_len(r), dtype=torch.float32, device="cuda")
+                 for r in range(4)]
+        c.s16 = [torch.empty(c.plan.shard_len(r), dtype=torch.bfloat16, device="cuda")
+                 for r in range(4)]
+        return c
+    ref = [make() for _ in range(4)]
+    got = [make() for _ in range(4)]
+    grads = [ref[0].grads(t) for t in (1, 2, 3)]     # read-only, shared by every thread
+
+    def run(c, k, stream, errors=None):
+        for i, t in enumerate((1, 2, 3)):
+            g = grads[i]
+            if k % 2:
+                Z.zero_step(c.plan, g, "avg", c.master, c.m, c.v, c.full16, None, HP, t,
+                            bucket_elems=7000 + 1000 * k, stream=stream)
+            else:
+                Z.zero_reduce_scatter(c.plan, g, "avg", c.gsh, stream=stream)
+                Z.zero_adamw_shard_step(c.plan, c.master, c.m, c.v, c.gsh, c.s16, HP, t,
+                                        stream=stream)
+                Z.zero_allgather(c.plan, c.s16, c.full16, stream=stream)
+        if errors is not None:
+            try:
+                Z.zero_step(c.plan, grads[0], "avg", c.master, c.m, c.v, c.full16, None, HP,
+                            -k, stream=stream)
+            except Z.ZeroError as e:
+                errors[k] = str(e)
+
+    for k in range(4):
+        run(ref[k], k, None)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    errors = [None] * 4
+    threads = [threading.Thread(target=run, args=(got[k], k, streams[k], errors))
+               for k in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    for k in range(4):
+        for r in range(4):
+            assert torch.equal(got[k].master[r], ref[k].master[r]), (k, r)
+            assert torch.equal(got[k].m[r], ref[k].m[r]), (k, r)
+            assert torch.equal(got[k].v[r], ref[k].v[r]), (k, r)
+        assert torch.equal(got[k].full16, ref[k].full16), k
+        # each thread's message names its own bad step number
+        assert errors[k] is not None and f"got {-k}" in errors[k], errors[k]
+
+
 def test_init_shards_exact():
     w = W.small((1000, 37, 4096, 3), 3, mode="flat", align=2, dtype="bf16")
     c = Case(w)
