@@ -8,7 +8,10 @@
  * mixed-precision step twice over -- zero_step_amp, and the bucket
  * reductions that write the norm's partial sums followed by
  * zero_step_amp_reduced -- requires the two to agree bit for bit and both
- * to match the oracle's mixed-precision step.
+ * to match the oracle's mixed-precision step; mode "offload" runs
+ * zero_offload_step with the optimizer state in plain malloc'd host memory
+ * and the gradient / 16-bit shards in cudaHostAlloc'd memory, two steps in
+ * ragged chunks on 3 host threads, against the oracle.
  *
  * Exit status 0 on success; prints the first mismatch otherwise.
  */
@@ -297,8 +300,90 @@ static int amp_checks(void) {
   return 0;
 }
 
+static int offload_checks(void) {
+  zero_plan* plan = NULL;
+  CHECK(zero_plan_partitions(kNumel, kTensors, kRanks, ZERO_PART_FLAT, kAlign, &plan) == ZERO_OK,
+        "plan");
+  int64_t phi, P, S, off;
+  zero_plan_total(plan, &phi, &P);
+  zero_plan_shard(plan, 0, &off, &S);
+  uint16_t* p16 = calloc((size_t)P, 2);
+  uint16_t* g16[2][kRanks];
+  uint32_t seed = 777u;
+  for (int64_t i = 0; i < phi; ++i)
+    p16[i] = orc_f32_to_bf16(((float)(lcg(&seed) >> 8) / 16777216.0f - 0.5f) * 0.05f);
+  for (int t = 0; t < 2; ++t)
+    for (int q = 0; q < kRanks; ++q) {
+      g16[t][q] = calloc((size_t)P, 2);
+      for (int64_t i = 0; i < phi; ++i)
+        g16[t][q][i] = orc_f32_to_bf16(((float)(lcg(&seed) >> 8) / 16777216.0f - 0.5f) * 0.02f);
+    }
+  /* device: the replicas and the gathered buffer; host: everything else */
+  void *d_full, *d_g[kRanks];
+  float *h_master[kRanks], *h_m[kRanks], *h_v[kRanks], *h_gsh[kRanks];
+  void* h_s16[kRanks];
+  CHECK(cudaMalloc(&d_full, (size_t)P * 2) == cudaSuccess, "cudaMalloc");
+  for (int r = 0; r < kRanks; ++r) {
+    CHECK(cudaMalloc(&d_g[r], (size_t)P * 2) == cudaSuccess, "cudaMalloc");
+    CHECK((h_master[r] = aligned_alloc(64, (size_t)S * 4)) != NULL, "aligned_alloc");
+    CHECK((h_m[r] = calloc((size_t)S, 4)) != NULL, "calloc");
+    CHECK((h_v[r] = calloc((size_t)S, 4)) != NULL, "calloc");
+    CHECK(cudaHostAlloc((void**)&h_gsh[r], (size_t)S * 4, cudaHostAllocDefault) == cudaSuccess,
+          "cudaHostAlloc");
+    CHECK(cudaHostAlloc(&h_s16[r], (size_t)S * 2, cudaHostAllocDefault) == cudaSuccess,
+          "cudaHostAlloc");
+    for (int64_t i = 0; i < S; ++i) h_master[r][i] = orc_bf16_to_f32(p16[r * S + i]);
+  }
+  float *o_master[kRanks], *o_m[kRanks], *o_v[kRanks];
+  for (int r = 0; r < kRanks; ++r) {
+    o_master[r] = malloc((size_t)S * 4);
+    o_m[r] = calloc((size_t)S, 4);
+    o_v[r] = calloc((size_t)S, 4);
+    memcpy(o_master[r], h_master[r], (size_t)S * 4);
+  }
+  uint16_t* o_full = calloc((size_t)P, 2);
+  zero_adamw_hparams hp = {1e-3, 0.9, 0.999, 1e-8, 0.01};
+  orc_hparams ohp = {1e-3, 0.9, 0.999, 1e-8, 0.01};
+  /* pageable gradient shards are refused before anything is launched */
+  float* pageable[kRanks];
+  for (int r = 0; r < kRanks; ++r) pageable[r] = h_m[r];
+  const int64_t before = zero_launch_count();
+  CHECK(zero_offload_step(plan, (const void* const*)d_g, ZERO_BF16, ZERO_REDUCE_AVG, pageable,
+                          h_master, h_m, h_v, h_s16, d_full, &hp, 1, 0xF, 1000, 3,
+                          NULL) == ZERO_ERR_INVALID, "pageable gradient shards were accepted");
+  CHECK(zero_launch_count() == before, "a refused call launched");
+  for (int t = 0; t < 2; ++t) {
+    for (int q = 0; q < kRanks; ++q)
+      cudaMemcpy(d_g[q], g16[t][q], (size_t)P * 2, cudaMemcpyHostToDevice);
+    CHECK(zero_offload_step(plan, (const void* const*)d_g, ZERO_BF16, ZERO_REDUCE_AVG, h_gsh,
+                            h_master, h_m, h_v, h_s16, d_full, &hp, t + 1, 0xF, 1000, 3,
+                            NULL) == ZERO_OK, "offload step: %s", zero_last_error());
+    CHECK(orc_step(kNumel, kTensors, kRanks, 0, kAlign, 1, 1, (const uint16_t* const*)g16[t],
+                   o_master, o_m, o_v, o_full, NULL, &ohp, t + 1, 0xF) == 0, "oracle step");
+  }
+  CHECK(zero_sync(NULL) == ZERO_OK, "sync: %s", zero_last_error());
+  uint16_t* full = malloc((size_t)P * 2);
+  cudaMemcpy(full, d_full, (size_t)P * 2, cudaMemcpyDeviceToHost);
+  for (int64_t i = 0; i < P; ++i)
+    CHECK(full[i] == o_full[i], "full16[%lld]: %04x vs oracle %04x", (long long)i, full[i],
+          o_full[i]);
+  for (int r = 0; r < kRanks; ++r) {
+    CHECK(memcmp(h_s16[r], o_full + r * S, (size_t)S * 2) == 0, "host shard16[%d]", r);
+    for (int64_t i = 0; i < S; ++i) {
+      const double a = h_master[r][i], b = o_master[r][i];
+      const double rel = fabs(a - b) / fmax(fabs(b), 1.1754943508222875e-38);
+      CHECK(rel <= 1e-6, "master[%d][%lld]: %.9g vs oracle %.9g", r, (long long)i, a, b);
+    }
+  }
+  printf("offload ok: %lld elements, host state, chunks of 1000 on 3 host threads, 2 steps "
+         "match the oracle\n", (long long)P);
+  zero_plan_destroy(plan);
+  return 0;
+}
+
 int main(int argc, char** argv) {
   if (argc > 1 && strcmp(argv[1], "gpu") == 0) return gpu_checks();
   if (argc > 1 && strcmp(argv[1], "amp") == 0) return amp_checks();
+  if (argc > 1 && strcmp(argv[1], "offload") == 0) return offload_checks();
   return host_checks();
 }

@@ -9,6 +9,9 @@ gathered bf16 buffer bit-identical to the oracle and the fp32 masters within
 1e-6 relative.  "amp" mode: the mixed-precision step from C, fused and as
 bucket reductions (last bucket first) plus zero_step_amp_reduced, the two
 bit-identical and both matching the oracle's mixed-precision step.
+"offload" mode: zero_offload_step with malloc'd host state and cudaHostAlloc'd
+shards, in ragged chunks on 3 host threads, against the oracle; pageable
+gradient shards are refused without a launch.
 """
 import glob
 import os
@@ -70,3 +73,11 @@ def test_c_program_mixed_precision_paths_match_oracle(program):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     assert "amp ok" in _run(program, "amp")
+
+
+@pytest.mark.gpu
+def test_c_program_offload_step_matches_oracle(program):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    assert "offload ok" in _run(program, "offload")
