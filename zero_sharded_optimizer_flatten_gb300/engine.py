@@ -39,7 +39,8 @@ still takes the decision and the host applies it,
 ``zero_offload_step_amp``).  ``offload="host_state"`` keeps the update on
 the GPU, whose kernels read and write the host-resident master/m/v across
 NVLink-C2C (no host synchronisation).  Both give the device engine's results
-bit for bit.
+bit for bit.  ``host_threads`` sets the CPU optimizer's threads (0: every
+hardware thread but one).
 
 The arithmetic is the library's (no compute happens here); this module only
 does bookkeeping and launches.
