@@ -153,3 +153,44 @@ def test_random_group_unfused_calls_match_oracle(seed):
             assert_fp32_close(f32(c.v[r]), c.o_v[r], f"{what} v[{r}]")
     if shard_out:
         assert_16_close(u16(c.full16), c.o_full, f"{what} full16", dtype_code=dt_code(w))
+
+
+@pytest.mark.parametrize("seed", range(1, N_CASES, 4))
+def test_random_group_offload_step(seed):
+    """zero_offload_step on the same random draws (masks, N up to 64, both
+    layouts), with a random chunk size and thread count: the host state,
+    the host 16-bit shards and the gathered buffer against the oracle's
+    step, two steps."""
+    w, _, _, hp = draw_case(seed)
+    rng = np.random.default_rng(9000 + seed)
+    c = Case(w)
+    P = c.plan.padded
+    # 0: one chunk; else a chunk size that leaves at most 4000 chunks
+    chunk = max(int(rng.integers(1, P + 2)), -(-P // 4000)) if rng.random() < 0.8 else 0
+    threads = int(rng.integers(1, 9))
+    what = (f"seed {seed}: numel {w.numel} N={w.n_ranks} {w.mode} A={w.align} {w.dtype} "
+            f"{w.op} mask={w.mask:#x} chunk={chunk} threads={threads}")
+    S = [c.plan.shard_len(r) if (w.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+    hm = [x.cpu() for x in c.master]
+    hmm = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hv = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hg = [torch.zeros(n, dtype=torch.float32, pin_memory=True) if n else 0 for n in S]
+    h16 = [torch.zeros(n, dtype=w.torch_dtype, pin_memory=True) if n else 0 for n in S]
+    for t in (1, 2):
+        g = c.grads(t)
+        Z.zero_offload_step(c.plan, g, w.op, hg, hm, hmm, hv, h16, c.full16, hp, t,
+                            rank_mask=w.mask, chunk_elems=chunk, n_threads=threads)
+        oracle.step(list(w.numel), w.n_ranks, mode_code(w), w.align, dt_code(w), op_code(w),
+                    [u16(x) for x in g], c.o_master, c.o_m, c.o_v, c.o_full, None,
+                    hp_oracle(hp), t, w.mask)
+    torch.cuda.synchronize()
+    for r in range(w.n_ranks):
+        if not S[r]:
+            continue
+        assert_fp32_close(hm[r].numpy(), c.o_master[r], f"{what} master[{r}]")
+        assert_fp32_close(hmm[r].numpy(), c.o_m[r], f"{what} m[{r}]")
+        assert_fp32_close(hv[r].numpy(), c.o_v[r], f"{what} v[{r}]")
+        seg = c.o_seg[r]
+        want = np.concatenate([c.o_full[f:f + n] for _, _, f, _, n in seg])
+        assert_16_close(u16(h16[r]), want, f"{what} shard16[{r}]", dtype_code=dt_code(w))
+    assert_16_close(u16(c.full16), c.o_full, f"{what} full16", dtype_code=dt_code(w))
