@@ -262,6 +262,47 @@ def test_amp_random_groups(seed):
                 assert torch.equal(x[r].view(torch.int32), y[r].view(torch.int32)), (seed, t, r)
 
 
+@pytest.mark.parametrize("seed", range(0, 12, 3))
+def test_amp_random_groups_offloaded(seed):
+    """The same random draws and controls through zero_offload_step_amp
+    (host state, random chunk size and thread count): bit for bit the
+    device-resident zero_step_amp over five calls, skipped overflows
+    included."""
+    from tests.test_gpu_fuzz import draw_case
+    w, bucket, _, _ = draw_case(100 + seed)
+    rng = np.random.default_rng(9000 + seed)
+    cfg = Z.AmpConfig(init_scale=float(rng.choice([1.0, 2.0 ** 8, 2.0 ** 16, 2.0 ** 24])),
+                      min_scale=1.0, window=int(rng.choice([0, 1, 2, 1000])),
+                      hysteresis=int(rng.choice([1, 2, 3])),
+                      max_norm=float(rng.choice([0.0, 1e-3, 0.05, 10.0])))
+    ref = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    got = AmpCase(w, cfg, bucket=bucket, with_oracle=False)
+    P = ref.plan.padded
+    chunk = max(int(rng.integers(1, P + 2)), -(-P // 4000))
+    threads = int(rng.integers(1, 9))
+    S = [got.plan.shard_len(r) if (w.mask >> r) & 1 else 0 for r in range(w.n_ranks)]
+    hm = [x.cpu() for x in got.master]
+    hmm = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hv = [torch.zeros(n, dtype=torch.float32) for n in S]
+    hg = [torch.zeros(n, dtype=torch.float32, pin_memory=True) if n else 0 for n in S]
+    h16 = [torch.zeros(n, dtype=w.torch_dtype, pin_memory=True) if n else 0 for n in S]
+    scale = cfg.init_scale
+    for t in range(1, 6):
+        g = ref.grads_scaled(t, scale)
+        ref.gpu_step(g)
+        Z.zero_offload_step_amp(got.plan, g, w.op, hg, hm, hmm, hv, h16, got.full16, HP, cfg,
+                                got.state, got.ws, rank_mask=w.mask, bucket_elems=bucket,
+                                chunk_elems=chunk, n_threads=threads)
+        torch.cuda.synchronize()
+        assert torch.equal(ref.state, got.state), (seed, t)
+        assert torch.equal(ref.full16.view(torch.int16), got.full16.view(torch.int16)), (seed, t)
+        for r in range(w.n_ranks):
+            if S[r]:
+                for x, y in ((ref.master, hm), (ref.m, hmm), (ref.v, hv)):
+                    assert torch.equal(x[r].cpu().view(torch.int32), y[r].view(torch.int32)), \
+                        (seed, t, r)
+        scale = Z.read_amp_state(ref.state).scale
+
 def test_amp_many_tensors_number_tiles_across_launches():
     """700 round-robin tensors: the reduction needs several launches per call
     and each numbers its tiles after the previous ones (the per-tile sums
