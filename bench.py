@@ -357,16 +357,23 @@ def run_reference(args, world, rank):
         els.append(sample.step(t))
     tot = sum(els)
     value = n * args.steps / tot
+    # the elements one step of the GPU arm updates: the masked ranks' shards
+    # (the oracle's own plan)
+    import oracle
+    mode = oracle.FLAT if w.mode == "flat" else oracle.ROUND_ROBIN
+    units = sum(oracle.shard_len(list(w.numel), w.n_ranks, mode, w.align, r)
+                for r in range(w.n_ranks) if (w.mask >> r) & 1)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.title, "phi": w.phi,
+        "config": {"workload": w.title, "phi": w.phi, "elements_per_step": units,
                    "virtual_ranks": w.n_ranks, "sample_elements_per_step": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "host": host_cpu(),
-                         "sample": f"{n} of {w.phi} elements per step, single-threaded C oracle"},
+                         "sample": f"the first {n} of the {units} elements one step updates "
+                                   "(all gradient replicas), single-threaded C oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
