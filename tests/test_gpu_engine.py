@@ -188,3 +188,49 @@ def test_engine_mixed_precision_with_offload(offload):
 def test_engine_offload_arguments():
     with pytest.raises(ValueError):
         ZeroEngine(_mlp(torch.bfloat16).parameters(), 2, offload="nvme")
+
+
+@pytest.mark.parametrize("amp,offload", [(False, None), (True, None), (False, "cpu"),
+                                         (False, "host_state"), (True, "host_state")])
+def test_engine_checkpoint_resume_is_bit_identical(amp, offload):
+    """state_dict() after three iterations, load_state_dict() into a fresh
+    engine over a differently initialised model, two more iterations: the
+    parameters and the optimizer (and mixed-precision) state equal those of
+    five uninterrupted iterations bit for bit."""
+    dtype = torch.float16 if amp else torch.bfloat16
+    cfg = (Z.AmpConfig(init_scale=2.0 ** 24, min_scale=1.0, window=2, hysteresis=1,
+                       max_norm=1.0) if amp else None)
+
+    def engine(model):
+        return ZeroEngine(model.parameters(), 4, bucket_elems=60_000, amp=cfg, offload=offload)
+
+    def iterate(eng, model, t):
+        for q in range(4):
+            eng.backward(_loss(model, _batch(q, t, dtype)), q)
+        eng.step()
+
+    a = _mlp(dtype)
+    ea = engine(a)
+    for t in range(1, 6):
+        iterate(ea, a, t)
+    b = _mlp(dtype)
+    eb = engine(b)
+    for t in range(1, 4):
+        iterate(eb, b, t)
+    sd = eb.state_dict()
+    c = _mlp(dtype, seed=5)
+    ec = engine(c)
+    with pytest.raises(ValueError):
+        ZeroEngine(_mlp(dtype).parameters(), 2).load_state_dict(sd)
+    ec.load_state_dict(sd)
+    for t in range(4, 6):
+        iterate(ec, c, t)
+    torch.cuda.synchronize()
+    assert torch.equal(ea.flat16, ec.flat16)
+    for r in range(4):
+        for x, y in ((ea.master[r], ec.master[r]), (ea.m[r], ec.m[r]), (ea.v[r], ec.v[r])):
+            assert torch.equal(x.cpu(), y.cpu())
+    if amp:
+        assert torch.equal(ea.amp_state, ec.amp_state)
+        assert Z.read_amp_state(ea.amp_state).skipped >= 1
+    assert ec.step_count == ea.step_count == 5

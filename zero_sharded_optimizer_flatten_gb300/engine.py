@@ -238,6 +238,49 @@ class ZeroEngine:
             Z.zero_allgather(self.plan, self.shard16, self.flat16)
         self._reset()
 
+    def state_dict(self) -> dict:
+        """Host copies of everything a resumed run needs: the fp32 master, m
+        and v of every rank, the 16-bit flat parameters, the step count and
+        the mixed-precision state (the checkpoint of the optimizer; saving it
+        is the caller's, e.g. torch.save)."""
+        # host-resident state is written by the device (offload='host_state')
+        # or read by its gathers: wait for every stream before copying
+        torch.cuda.synchronize(self.flat16.device)
+
+        def host(xs):
+            return [x.detach().cpu().clone() for x in xs]
+        sd = {"numel": list(self.numel), "n_ranks": self.n_ranks, "mode": self.plan.mode,
+              "align": self.plan.align, "step_count": self.step_count,
+              "master": host(self.master), "m": host(self.m), "v": host(self.v),
+              "flat16": self.flat16.detach().cpu().clone()}
+        if self.amp is not None:
+            sd["amp_state"] = self.amp_state.detach().cpu().clone()
+        return sd
+
+    def load_state_dict(self, sd: dict):
+        """Restore a state_dict() of an engine over the same parameter group:
+        the model's parameters (views of the flat buffer) and the optimizer
+        state take the saved values, so training continues bit for bit."""
+        same = (list(sd["numel"]) == list(self.numel) and sd["n_ranks"] == self.n_ranks
+                and sd["mode"] == self.plan.mode and sd["align"] == self.plan.align)
+        if not same:
+            raise ValueError("the checkpoint was taken over another parameter group or plan")
+        if ("amp_state" in sd) != (self.amp is not None):
+            raise ValueError("the checkpoint and the engine disagree on amp")
+        torch.cuda.synchronize(self.flat16.device)   # no kernel still uses the old state
+        with torch.no_grad():
+            for key in ("master", "m", "v"):
+                for dst, src in zip(getattr(self, key), sd[key]):
+                    if dst.shape != src.shape:
+                        raise ValueError(f"{key}: shard of {tuple(src.shape)}, expected "
+                                         f"{tuple(dst.shape)}")
+                    dst.copy_(src)
+            self.flat16.copy_(sd["flat16"])
+            if self.amp is not None:
+                self.amp_state.copy_(sd["amp_state"])
+        self.step_count = int(sd["step_count"])
+        self._reset()
+
     def amp_status(self) -> "Z.AmpState":
         """The mixed-precision state (loss scale, last norm, steps taken and
         skipped); copying it to the host synchronises with the stream."""
