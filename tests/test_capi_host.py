@@ -186,3 +186,57 @@ def test_selftest_rejects_bad_limits(L):
     for bad in (0, 999, 10**11):
         assert L.zero_selftest_wait_timeout(bad, None) == Z.ZERO_ERR_INVALID
     assert Z.zero_launch_count() == before
+
+
+def test_more_calls_reject_bad_arguments_without_launching(L):
+    """The range reduction, the ZeRO-3 pass, the offload steps and the
+    reduced mixed-precision step refuse bad arguments with the documented
+    status before any CUDA call (this host has no GPU), and launch nothing."""
+    plan = Z.zero_plan_partitions([100, 28], 2, "flat", 16)     # padded 128, 2 shards of 64
+    good = 1 << 20
+    p2 = _arr([good, good])
+    hp = Z.AdamW().c()
+    cfg = Z.AmpConfig().c()
+    before = Z.zero_launch_count()
+    # a flat range outside [0, padded]
+    for lo, hi in ((-1, 10), (10, 5), (0, 129)):
+        assert L.zero_reduce_scatter_range(plan.handle, p2, 1, 1, p2, 3, lo, hi,
+                                           None) == Z.ZERO_ERR_INVALID
+    assert "range" in Z.zero_last_error()
+    # the ZeRO-3 pass: no layer, no or too many buffers, a NULL or misaligned buffer
+    layer = Z._LayerC(p2, p2, p2, p2, p2)
+    one = (Z._LayerC * 1)(layer)
+    assert L.zero_zero3_pass(plan.handle, one, 0, p2, 1, 1, 1, ctypes.byref(hp), 1, None,
+                             None) == Z.ZERO_ERR_INVALID
+    for nb in (0, 65):
+        assert L.zero_zero3_pass(plan.handle, one, 1, p2, nb, 1, 1, ctypes.byref(hp), 1, None,
+                                 None) == Z.ZERO_ERR_INVALID
+    assert L.zero_zero3_pass(plan.handle, one, 1, _arr([0]), 1, 1, 1, ctypes.byref(hp), 1, None,
+                             None) == Z.ZERO_ERR_INVALID
+    assert L.zero_zero3_pass(plan.handle, one, 1, _arr([good + 2]), 1, 1, 1, ctypes.byref(hp),
+                             1, None, None) == Z.ZERO_ERR_ALIGN
+
+    # the offload steps: a bad op, step 0, a misaligned gathered buffer, no
+    # 16-bit shards, too many chunks
+    def offload(op=1, step=1, o16=p2, full=good):
+        return L.zero_offload_step(plan.handle, p2, 1, op, p2, p2, p2, p2, o16, full,
+                                   ctypes.byref(hp), step, 3, 0, 2, None)
+    assert offload(op=7) == Z.ZERO_ERR_INVALID
+    assert offload(step=0) == Z.ZERO_ERR_INVALID
+    assert offload(full=good + 2) == Z.ZERO_ERR_ALIGN
+    assert offload(o16=None) == Z.ZERO_ERR_INVALID
+    big = Z.zero_plan_partitions([5000], 2, "flat", 16)       # 5024 chunks of 1 element
+    assert L.zero_offload_step(big.handle, p2, 1, 1, p2, p2, p2, p2, p2, good, ctypes.byref(hp),
+                               1, 3, 1, 2, None) == Z.ZERO_ERR_INVALID
+    assert "chunks" in Z.zero_last_error()
+    assert L.zero_offload_step_amp(big.handle, p2, 1, 1, p2, p2, p2, p2, p2, good,
+                                   ctypes.byref(hp), ctypes.byref(cfg), good, good, 1 << 20, 3, 0,
+                                   1, 2, None) == Z.ZERO_ERR_INVALID
+    assert "chunks" in Z.zero_last_error()
+    # the reduced mixed-precision step with a workspace that is too small
+    need = Z.zero_amp_workspace_bytes(plan)
+    assert L.zero_step_amp_reduced(plan.handle, 1, p2, p2, p2, p2, good, None, ctypes.byref(hp),
+                                   ctypes.byref(cfg), good, good, need - 16, 3, 0,
+                                   None) == Z.ZERO_ERR_INVALID
+    assert "workspace" in Z.zero_last_error()
+    assert Z.zero_launch_count() == before
